@@ -1,0 +1,172 @@
+"""Exact softmax attention for NVIDIA GB300 (sm_103a): Python binding.
+
+A thin ctypes layer over the C ABI in ``include/attn.h`` (``libattn_sm103.so``,
+built in-tree by ``exact_attention_95_gb300.build``).  It only marshals
+arguments: PyTorch supplies device memory and the current stream, and every
+step of the computation runs in the library's CUDA kernels.  If the library
+is missing, every call raises; there is no fallback implementation.
+
+Functions carry the C names:
+
+* ``attn_fwd(Q, K, V, scale, causal, out_dtype=None) -> (O, LSE)``
+* ``attn_bwd(Q, K, V, O, dO, LSE, scale, causal) -> (dQ, dK, dV)``
+* ``attn_bwd_workspace_size(B, Hq, Hkv, N, d)``
+* ``attn_last_device_status(stream=None)``, ``attn_status_string(code)``
+* ``attn_selftest_wait_timeout(limit_ns)``
+
+Tensors are ``[B, H, N, d]`` contiguous CUDA tensors (bf16, or fp32 for the
+fp32 forward); ``LSE`` is ``[B, Hq, N]`` fp32.
+"""
+
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn_sm103.so")
+
+ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
+ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5
+ATTN_BF16, ATTN_F32 = 0, 1
+
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string",
+            "attn_last_device_status", "attn_selftest_wait_timeout")
+
+_lock = threading.Lock()
+_lib = None
+
+
+class AttnError(RuntimeError):
+    def __init__(self, code: int, where: str):
+        self.code = code
+        super().__init__(f"{where}: {attn_status_string(code)}")
+
+
+def load_library(path: str = LIB_PATH):
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(path):
+            raise RuntimeError(
+                f"CUDA library {path} is missing; build it with "
+                "`python -m exact_attention_95_gb300.build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(path)
+        vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+        lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, i32, vp]
+        lib.attn_fwd.restype = i32
+        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                                 i32, i32, vp, sz, vp]
+        lib.attn_bwd.restype = i32
+        lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
+        lib.attn_bwd_workspace_size.restype = sz
+        lib.attn_status_string.argtypes = [i32]
+        lib.attn_status_string.restype = ctypes.c_char_p
+        lib.attn_last_device_status.argtypes = [vp]
+        lib.attn_last_device_status.restype = i32
+        lib.attn_selftest_wait_timeout.argtypes = [ctypes.c_ulonglong, vp]
+        lib.attn_selftest_wait_timeout.restype = i32
+        _lib = lib
+        return lib
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_tensor(name, t, dtype, shape):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def attn_status_string(code: int) -> str:
+    return load_library().attn_status_string(int(code)).decode()
+
+
+def attn_bwd_workspace_size(B: int, Hq: int, Hkv: int, N: int, d: int) -> int:
+    return int(load_library().attn_bwd_workspace_size(B, Hq, Hkv, N, d))
+
+
+def attn_last_device_status(stream=None) -> int:
+    return int(load_library().attn_last_device_status(_stream(stream)))
+
+
+def attn_selftest_wait_timeout(limit_ns: int, stream=None) -> int:
+    return int(load_library().attn_selftest_wait_timeout(int(limit_ns), _stream(stream)))
+
+
+def attn_fwd(Q, K, V, scale=None, causal=False, out_dtype=None, O=None, LSE=None, stream=None):
+    """O, LSE = softmax(scale Q K^T [+causal]) V and its row log-sum-exp."""
+    lib = load_library()
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    in_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}.get(Q.dtype)
+    if in_dt is None:
+        raise TypeError("Q must be bf16 or fp32")
+    if out_dtype is None:
+        out_dtype = Q.dtype
+    out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
+    _check_tensor("Q", Q, Q.dtype, (B, Hq, N, d))
+    _check_tensor("K", K, Q.dtype, (B, Hkv, N, d))
+    _check_tensor("V", V, Q.dtype, (B, Hkv, N, d))
+    if O is None:
+        O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Q.device)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
+    rc = lib.attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                      float(scale), int(bool(causal)), in_dt, out_dt, _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd")
+    return O, LSE
+
+
+def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV=None,
+             workspace=None, stream=None):
+    """dQ, dK, dV of O = attention(Q, K, V) given dO and the forward's LSE."""
+    lib = load_library()
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bf = torch.bfloat16
+    _check_tensor("Q", Q, bf, (B, Hq, N, d))
+    _check_tensor("K", K, bf, (B, Hkv, N, d))
+    _check_tensor("V", V, bf, (B, Hkv, N, d))
+    _check_tensor("O", O, bf, (B, Hq, N, d))
+    _check_tensor("dO", dO, bf, (B, Hq, N, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d)
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+    rc = lib.attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
+                      _ptr(dV), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), ATTN_BF16,
+                      _ptr(workspace), workspace.numel() * workspace.element_size(),
+                      _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd")
+    return dQ, dK, dV

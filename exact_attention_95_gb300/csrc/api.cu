@@ -1,0 +1,243 @@
+// api.cu -- the C ABI declared in include/attn.h: argument checks, TMA
+// tensor-map construction, kernel launches and the device status word.
+#include <cmath>
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+
+// Device status word: kernels record the first failure of a launch here
+// (atomicCAS from 0); attn_last_device_status reads and clears it.
+__device__ int g_status = 0;
+
+namespace {
+
+constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                   const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                   const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// Device address of the status word on the current device.
+int* status_ptr() {
+  static int* ptrs[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!ptrs[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) return nullptr;
+    ptrs[dev] = static_cast<int*>(p);
+  }
+  return ptrs[dev];
+}
+
+// 3-D map over a bf16 [BH][N][d] tensor: box of 64 columns (128 bytes, the
+// 128-byte swizzle width) x box_rows rows x 1 head.  Rows past N read as zero.
+bool make_map(CUtensorMap* m, const void* base, long long BH, int N, int d, int box_rows) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
+            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Shape checks shared by forward and backward.  Returns ATTN_OK or an error.
+attn_status check_shape(int B, int Hq, int Hkv, int N, int d, float scale, int causal) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
+  if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  // Grid limits: query tiles on grid.y, (b, h) on grid.x; element counts fit int64.
+  if ((N + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
+  if ((long long)B * Hq > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  return ATTN_OK;
+}
+
+unsigned long long wait_limit() { return kDefaultWaitLimitNs; }
+
+// Diagnostic kernel: one thread waits on an mbarrier that is never completed.
+__global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x == 0) {
+    mbar_init(smem_u32(&bar), 1);
+    abort_flag = 0;
+    fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    WaitCtx wc{&abort_flag, status, limit_ns};
+    mbar_wait(smem_u32(&bar), 0, wc);
+  }
+}
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" {
+
+const char* attn_status_string(attn_status s) {
+  switch (s) {
+    case ATTN_OK: return "ATTN_OK";
+    case ATTN_ERR_INVALID_ARG: return "ATTN_ERR_INVALID_ARG";
+    case ATTN_ERR_UNSUPPORTED: return "ATTN_ERR_UNSUPPORTED";
+    case ATTN_ERR_CUDA: return "ATTN_ERR_CUDA";
+    case ATTN_ERR_TIMEOUT: return "ATTN_ERR_TIMEOUT";
+    case ATTN_ERR_DEVICE: return "ATTN_ERR_DEVICE";
+  }
+  return "ATTN_UNKNOWN_STATUS";
+}
+
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype in_dtype, attn_dtype out_dtype, void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if ((in_dtype != ATTN_BF16 && in_dtype != ATTN_F32) ||
+      (out_dtype != ATTN_BF16 && out_dtype != ATTN_F32))
+    return ATTN_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_shape(B, Hq, Hkv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float sl2 = scale * 1.4426950408889634f;
+  if (in_dtype == ATTN_F32) {
+    if (out_dtype != ATTN_F32) return ATTN_ERR_UNSUPPORTED;
+    cudaError_t e = launch_fwd_f32(d, static_cast<const float*>(Q), static_cast<const float*>(K),
+                                   static_cast<const float*>(V), static_cast<float*>(O), LSE, B, Hq,
+                                   Hkv, N, sl2, causal, s);
+    return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+  }
+  int* status = status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, Q, (long long)B * Hq, N, d, 128) || !make_map(&tk, K, (long long)B * Hkv, N, d, 128) ||
+      !make_map(&tv, V, (long long)B * Hkv, N, d, 128))
+    return ATTN_ERR_CUDA;
+  FwdParams p{};
+  p.O = O;
+  p.LSE = LSE;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.n_qtiles = (N + 127) / 128;
+  p.scale_log2 = sl2;
+  p.causal = causal;
+  p.out_f32 = out_dtype == ATTN_F32 ? 1 : 0;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e = launch_fwd_bf16(d, tq, tk, tv, p, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
+  if (check_shape(B, Hq, Hkv, N, d, 1.0f, 0) != ATTN_OK) return 0;
+  return bwd_workspace_bytes(B, Hq, N, d);
+}
+
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
+    return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (!aligned(q, 16)) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(LSE, 4) || !aligned(workspace, 256)) return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_shape(B, Hq, Hkv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (dtype != ATTN_BF16) return ATTN_ERR_UNSUPPORTED;
+  if (workspace_bytes < bwd_workspace_bytes(B, Hq, N, d)) return ATTN_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv, tdo;
+  if (!make_map(&tq, Q, (long long)B * Hq, N, d, 64) || !make_map(&tdo, dO, (long long)B * Hq, N, d, 64) ||
+      !make_map(&tk, K, (long long)B * Hkv, N, d, 128) || !make_map(&tv, V, (long long)B * Hkv, N, d, 128))
+    return ATTN_ERR_CUDA;
+  const int Npad = (N + 63) / 64 * 64;
+  BwdParams p{};
+  p.Q = static_cast<const uint16_t*>(Q);
+  p.K = static_cast<const uint16_t*>(K);
+  p.V = static_cast<const uint16_t*>(V);
+  p.O = static_cast<const uint16_t*>(O);
+  p.dO = static_cast<const uint16_t*>(dO);
+  p.LSE = LSE;
+  p.dQ = static_cast<uint16_t*>(dQ);
+  p.dK = static_cast<uint16_t*>(dK);
+  p.dV = static_cast<uint16_t*>(dV);
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t rows = (size_t)B * Hq * Npad;
+  const size_t acc_bytes = (rows * d * 4 + 255) / 256 * 256;
+  const size_t vec_bytes = (rows * 4 + 255) / 256 * 256;
+  p.dQacc = reinterpret_cast<float*>(ws);
+  p.Dvec = reinterpret_cast<float*>(ws + acc_bytes);
+  p.LSE2 = reinterpret_cast<float*>(ws + acc_bytes + vec_bytes);
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.Npad = Npad;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e = launch_bwd_bf16(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_last_device_status(void* stream) {
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return ATTN_ERR_CUDA;
+  int* p = status_ptr();
+  if (!p) return ATTN_ERR_CUDA;
+  int v = 0, zero = 0;
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return ATTN_ERR_CUDA;
+  if (v != 0 && cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess)
+    return ATTN_ERR_CUDA;
+  if (v == kDevTimeout) return ATTN_ERR_TIMEOUT;
+  return v == 0 ? ATTN_OK : ATTN_ERR_DEVICE;
+}
+
+attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream) {
+  if (limit_ns == 0 || limit_ns > 1000000000ull) return ATTN_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(status, limit_ns);
+  return cudaGetLastError() == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,114 @@
+// fwd_f32.cu -- exact attention forward in fp32 on CUDA cores.
+//
+// Same mathematics as the tensor-core forward (online max / sum merge of
+// "LLM 注意力与计算内核精读笔记 · 02 FlashAttention" §5, 1/l applied once),
+// carried out entirely in fp32 FFMA so that fp32 inputs keep fp32 accuracy.
+// The work is small (latency-bound); the kernel favours simplicity.
+//
+// Block: 128 threads.  TPR = d/32 consecutive threads share one query row,
+// each holding 32 of its d components of q and of the output accumulator.
+// Keys are streamed in tiles of 32 through shared memory; the partial dot
+// products of a row's TPR threads are combined with warp shuffles.
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kKT = 32;  // keys per shared-memory tile
+
+template <int D>
+__global__ void __launch_bounds__(128)
+    fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
+                   const float* __restrict__ V, float* __restrict__ O, float* __restrict__ LSE,
+                   int Hq, int Hkv, int N, float sl2, int causal) {
+  constexpr int TPR = D / 32;
+  constexpr int RPB = 128 / TPR;  // rows per block
+  constexpr int PAD = 33;         // padded 32-float segment (avoids bank conflicts)
+  __shared__ float Ks[kKT][TPR * PAD];
+  __shared__ float Vs[kKT][TPR * PAD];
+
+  const int bh = blockIdx.y;
+  const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
+  const int bh_kv = b * Hkv + h / (Hq / Hkv);
+  const int sub = threadIdx.x % TPR;
+  const int r = threadIdx.x / TPR;
+  const int q = blockIdx.x * RPB + r;
+  const bool valid = q < N;
+  const size_t qrow = (size_t)bh * N + (valid ? q : 0);
+
+  float qv[32], acc[32];
+#pragma unroll
+  for (int k = 0; k < 32; ++k) {
+    qv[k] = Q[qrow * D + sub * 32 + k];
+    acc[k] = 0.f;
+  }
+  float m = -INFINITY, l = 0.f;
+  const int q_last = min(N - 1, blockIdx.x * RPB + RPB - 1);
+  const int kend = causal ? q_last + 1 : N;
+  const float* Kh = K + (size_t)bh_kv * N * D;
+  const float* Vh = V + (size_t)bh_kv * N * D;
+  for (int k0 = 0; k0 < kend; k0 += kKT) {
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < kKT * D; idx += 128) {
+      const int kr = idx / D, c = idx - (idx / D) * D;
+      const bool in = k0 + kr < N;
+      Ks[kr][(c / 32) * PAD + (c % 32)] = in ? Kh[(size_t)(k0 + kr) * D + c] : 0.f;
+      Vs[kr][(c / 32) * PAD + (c % 32)] = in ? Vh[(size_t)(k0 + kr) * D + c] : 0.f;
+    }
+    __syncthreads();
+    float s[kKT];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < kKT; ++j) {
+      float part = 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) part = fmaf(qv[k], Ks[j][sub * PAD + k], part);
+#pragma unroll
+      for (int o = 1; o < TPR; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+      const int key = k0 + j;
+      const bool keep = key < N && (!causal || key <= q);
+      s[j] = keep ? part * sl2 : -INFINITY;
+      mx = fmaxf(mx, s[j]);
+    }
+    const float m_new = fmaxf(m, mx);
+    const float m_use = m_new == -INFINITY ? 0.f : m_new;
+    const float alpha = ex2(m - m_use);
+    float rs = 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) acc[k] *= alpha;
+#pragma unroll
+    for (int j = 0; j < kKT; ++j) {
+      const float pj = ex2(s[j] - m_use);
+      rs += pj;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) acc[k] = fmaf(pj, Vs[j][sub * PAD + k], acc[k]);
+    }
+    l = l * alpha + rs;
+    m = m_new;
+  }
+  if (valid) {
+    const float inv = l > 0.f ? 1.f / l : 0.f;
+#pragma unroll
+    for (int k = 0; k < 32; ++k) O[qrow * D + sub * 32 + k] = acc[k] * inv;
+    if (sub == 0) LSE[qrow] = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_fwd_f32(int d, const float* Q, const float* K, const float* V, float* O,
+                           float* LSE, int B, int Hq, int Hkv, int N, float scale_log2,
+                           int causal, cudaStream_t stream) {
+  const int rpb = 128 / (d / 32);
+  dim3 grid((N + rpb - 1) / rpb, B * Hq);
+  if (d == 64)
+    fwd_f32_kernel<64><<<grid, 128, 0, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
+  else if (d == 128)
+    fwd_f32_kernel<128><<<grid, 128, 0, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,62 @@
+// kernels.h -- internal launch interface between the C-ABI host code (api.cu)
+// and the kernels.  Not part of the public API.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+struct FwdParams {
+  void* O;          // [B, Hq, N, d] bf16 or fp32
+  float* LSE;       // [B, Hq, N] natural-log units
+  int* status;      // device status word
+  int B, Hq, Hkv, N;
+  int n_qtiles;     // ceil(N / 128)
+  float scale_log2; // scale * log2(e)
+  int causal;
+  int out_f32;
+  unsigned long long wait_limit_ns;
+};
+
+// tcgen05 forward for bf16 inputs.  tmQ/tmK/tmV are 3-D maps over
+// [B*H][N][d] with a (64, 128, 1) box and 128-byte swizzle.
+cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
+size_t fwd_bf16_smem_bytes(int d);
+
+// fp32 SIMT forward (exact fp32 arithmetic, FFMA + ex2).
+cudaError_t launch_fwd_f32(int d, const float* Q, const float* K, const float* V, float* O,
+                           float* LSE, int B, int Hq, int Hkv, int N, float scale_log2,
+                           int causal, cudaStream_t stream);
+
+struct BwdParams {
+  const uint16_t* Q;    // [B, Hq, N, d] bf16
+  const uint16_t* K;    // [B, Hkv, N, d]
+  const uint16_t* V;
+  const uint16_t* O;    // [B, Hq, N, d]
+  const uint16_t* dO;
+  const float* LSE;     // [B, Hq, N]
+  uint16_t* dQ;         // [B, Hq, N, d]
+  uint16_t* dK;         // [B, Hkv, N, d]
+  uint16_t* dV;
+  float* dQacc;         // workspace [B, Hq, Npad, d] fp32
+  float* Dvec;          // workspace [B, Hq, Npad]  rowsum(dO * O)
+  float* LSE2;          // workspace [B, Hq, Npad]  LSE * log2(e)
+  int* status;
+  int B, Hq, Hkv, N, Npad;
+  float scale;          // softmax scale
+  float scale_log2;     // scale * log2(e)
+  int causal;
+  unsigned long long wait_limit_ns;
+};
+
+// Workspace layout of the backward (bytes), all fp32: dQacc then D then LSE2.
+size_t bwd_workspace_bytes(int B, int Hq, int N, int d);
+
+cudaError_t launch_bwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                            const BwdParams& p, cudaStream_t stream);
+
+}  // namespace attn

@@ -1,0 +1,124 @@
+/*
+ * attn.h -- C ABI of the exact-attention library for NVIDIA GB300 (sm_103a).
+ *
+ * The library computes exact softmax attention
+ *
+ *     O = softmax(scale * Q K^T [+ causal mask]) V,     LSE_i = ln sum_j e^{s_ij},
+ *
+ * and its backward, with the tiled online-softmax method described in
+ * "LLM 注意力与计算内核精读笔记 · 02 FlashAttention：IO 感知的精确注意力"
+ * (§4 tiling, §5 online softmax merge, §6 recomputation) and in
+ * "[Attention优化][2w字]原理&图解: 从Online-Softmax到FlashAttention V1/V2/V3"
+ * (0x04 backward recomputation, 0x05 FlashAttention-2 loop order and the
+ * deferred 1/l, 0x09 GQA indexing and causal tiles).  The result is exact up
+ * to floating-point rounding: no approximation of the softmax is made.
+ *
+ * Data layout (all tensors): row-major [B, H, N, d], d contiguous.
+ *   Q, O, dO, dQ : H = Hq            K, V, dK, dV : H = Hkv
+ *   LSE          : [B, Hq, N] fp32, natural-log units of the scaled logits
+ * Query head h reads key/value head h / (Hq / Hkv) (contiguous groups).
+ * Causal masking keeps key j for query i when j <= i (Nq = Nk = N).
+ *
+ * Ownership: the caller owns every buffer; all pointers are device pointers
+ * unless stated otherwise.  The library allocates no device memory: the
+ * backward takes a caller-provided workspace.  Tensor pointers must be 16-byte
+ * aligned and LSE 4-byte aligned.
+ *
+ * Streams: `stream` is a cudaStream_t passed as void*; NULL means the legacy
+ * default stream.  Every call is asynchronous on that stream.  Argument and
+ * launch errors are returned synchronously; a device-side failure (a bounded
+ * wait inside a kernel that ran out) is recorded in a device status word and
+ * reported by attn_last_device_status().
+ *
+ * Errors: ATTN_ERR_INVALID_ARG for null or misaligned pointers, non-positive
+ * sizes, Hq % Hkv != 0, a non-finite scale or an unknown dtype;
+ * ATTN_ERR_UNSUPPORTED for combinations the kernels do not implement
+ * (d other than 64 or 128, fp32 backward, fp32 input with bf16 output);
+ * ATTN_ERR_CUDA when a CUDA runtime call or launch fails.  There is no CPU
+ * fallback.
+ */
+#ifndef EXACT_ATTENTION_GB300_ATTN_H
+#define EXACT_ATTENTION_GB300_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  ATTN_OK = 0,
+  ATTN_ERR_INVALID_ARG = 1,
+  ATTN_ERR_UNSUPPORTED = 2,
+  ATTN_ERR_CUDA = 3,
+  ATTN_ERR_TIMEOUT = 4,
+  ATTN_ERR_DEVICE = 5
+} attn_status;
+
+typedef enum { ATTN_BF16 = 0, ATTN_F32 = 1 } attn_dtype;
+
+/*
+ * Forward.  Per (batch b, query head h, query row i):
+ *   s_ij = scale * <Q[b,h,i,:], K[b,h/G,j,:]> for kept j,
+ *   O[b,h,i,:] = sum_j softmax_j(s_i) V[b,h/G,j,:],  LSE[b,h,i] = ln sum_j e^{s_ij}
+ * ("02 FlashAttention" §2 defines S, P, O; §5 the blockwise merge used).
+ *
+ *   Q [B,Hq,N,d], K and V [B,Hkv,N,d]   in_dtype (bf16: tensor-core path;
+ *                                       fp32: CUDA-core path)
+ *   O [B,Hq,N,d]                        out_dtype: bf16 or fp32 for bf16 input,
+ *                                       fp32 for fp32 input
+ *   LSE [B,Hq,N] fp32                   may not be NULL (the backward needs it)
+ *   B, Hq, Hkv, N >= 1; Hq % Hkv == 0; d in {64, 128}; causal in {0, 1}.
+ * O and LSE are fully overwritten.  Inputs are not modified.
+ */
+attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype in_dtype, attn_dtype out_dtype, void* stream);
+
+/*
+ * Backward of O with respect to Q, K, V given dO (no gradient through LSE).
+ * The probabilities are recomputed per tile from the saved LSE
+ * ("从Online-Softmax…" 0x04: recompute instead of storing S and P;
+ * "02 FlashAttention" §6), with K/V tiles in the outer loop and dQ
+ * accumulated across tiles (0x05).  With D_i = sum_k dO_ik O_ik:
+ *   dP_ij = <dO_i, v_j>,  dS_ij = p_ij (dP_ij - D_i),
+ *   dQ_i = scale sum_j dS_ij k_j,  dK_j = scale sum_{i, heads of group} dS_ij q_i,
+ *   dV_j = sum_{i, heads of group} p_ij dO_i.
+ *
+ *   Q, O, dO [B,Hq,N,d] bf16; K, V [B,Hkv,N,d] bf16; LSE [B,Hq,N] fp32 as
+ *   written by attn_fwd for the same Q, K, V, scale and causal.
+ *   dQ [B,Hq,N,d], dK, dV [B,Hkv,N,d] bf16: fully overwritten.
+ *   dtype must be ATTN_BF16 (fp32 backward: ATTN_ERR_UNSUPPORTED).
+ *   workspace: device memory of at least attn_bwd_workspace_size() bytes,
+ *   256-byte aligned, owned by the caller, contents need not be initialised;
+ *   it must not be shared with a concurrent call.
+ */
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Bytes of workspace attn_bwd needs: an fp32 dQ accumulator and two fp32
+ * per-row vectors (D = rowsum(dO * O) and LSE in log2 units).  0 on bad sizes. */
+size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
+
+/* Static string naming a status code. */
+const char* attn_status_string(attn_status s);
+
+/* Synchronises `stream`, then reads and clears the device status word of the
+ * current device.  Returns ATTN_ERR_TIMEOUT if a kernel's bounded wait ran out
+ * since the last call, ATTN_OK otherwise (ATTN_ERR_CUDA if the read fails). */
+attn_status attn_last_device_status(void* stream);
+
+/* Diagnostic: launches one CTA that waits, with the library's bounded-wait
+ * routine and a limit of `limit_ns` nanoseconds (at most 1e9), on an mbarrier
+ * that nothing will ever complete, then returns.  A working timeout path makes
+ * the following attn_last_device_status() report ATTN_ERR_TIMEOUT. */
+attn_status attn_selftest_wait_timeout(unsigned long long limit_ns, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* EXACT_ATTENTION_GB300_ATTN_H */

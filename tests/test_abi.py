@@ -1,0 +1,110 @@
+"""The C-ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host before touching the GPU (no GPU needed)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+import exact_attention_95_gb300 as pkg
+from exact_attention_95_gb300 import build as libbuild
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            src = open(os.path.join(ROOT, "include", fn), encoding="utf-8").read()
+            src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+            names += re.findall(r"^\s*[A-Za-z_][\w\s\*]*?\b(attn_\w+)\s*\(", src, flags=re.M)
+    return sorted(set(names))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return pkg.load_library()
+
+
+def test_every_declared_symbol_is_exported(lib):
+    names = _declared()
+    assert {"attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string",
+            "attn_last_device_status"} <= set(names)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(pkg.EXPORTED) == set(names)
+
+
+def test_status_strings(lib):
+    for code, name in [(0, "ATTN_OK"), (1, "ATTN_ERR_INVALID_ARG"), (2, "ATTN_ERR_UNSUPPORTED"),
+                       (3, "ATTN_ERR_CUDA"), (4, "ATTN_ERR_TIMEOUT"), (5, "ATTN_ERR_DEVICE")]:
+        assert pkg.attn_status_string(code) == name
+
+
+def test_workspace_size(lib):
+    # fp32 dQ accumulator over N rounded up to 64, plus two fp32 row vectors.
+    n = pkg.attn_bwd_workspace_size(2, 4, 2, 100, 64)
+    rows = 2 * 4 * 128
+    assert n == rows * 64 * 4 + 2 * rows * 4
+    assert pkg.attn_bwd_workspace_size(1, 3, 2, 100, 64) == 0  # Hq % Hkv
+    assert pkg.attn_bwd_workspace_size(1, 1, 1, 100, 96) == 0  # unsupported d
+
+
+A = ctypes.c_void_p(0x10000)  # fake, aligned; never dereferenced on these paths
+
+
+def _fwd(lib, **kw):
+    a = dict(Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=128, d=64, scale=0.125, causal=0,
+             ind=0, outd=0)
+    a.update(kw)
+    return lib.attn_fwd(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["Hq"], a["Hkv"],
+                        a["N"], a["d"], a["scale"], a["causal"], a["ind"], a["outd"], None)
+
+
+def test_fwd_argument_errors(lib):
+    assert _fwd(lib, Q=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, LSE=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, K=ctypes.c_void_p(0x10008)) == pkg.ATTN_ERR_INVALID_ARG  # misaligned
+    assert _fwd(lib, N=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, B=-1) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, Hq=3, Hkv=2) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=float("nan")) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, causal=2) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, ind=7) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, d=256) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, d=80) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, ind=pkg.ATTN_F32, outd=pkg.ATTN_BF16) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _fwd(lib, N=128 * 65536) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def _bwd(lib, **kw):
+    a = dict(ws=A, wsb=1 << 30, B=1, Hq=2, Hkv=1, N=128, d=64, dtype=0, causal=1)
+    a.update(kw)
+    return lib.attn_bwd(A, A, A, A, A, A, A, A, A, a["B"], a["Hq"], a["Hkv"], a["N"], a["d"],
+                        0.125, a["causal"], a["dtype"], a["ws"], a["wsb"], None)
+
+
+def test_bwd_argument_errors(lib):
+    assert _bwd(lib, ws=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert _bwd(lib, ws=ctypes.c_void_p(0x10010)) == pkg.ATTN_ERR_INVALID_ARG  # not 256-aligned
+    assert _bwd(lib, wsb=16) == pkg.ATTN_ERR_INVALID_ARG
+    assert _bwd(lib, Hq=4, Hkv=3) == pkg.ATTN_ERR_INVALID_ARG
+    assert _bwd(lib, d=32) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _bwd(lib, dtype=pkg.ATTN_F32) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _bwd(lib, dtype=9) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_missing_library_fails_loudly(tmp_path):
+    import importlib
+    mod = importlib.import_module("exact_attention_95_gb300")
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        # a fresh load from a path that does not exist
+        saved = mod._lib
+        try:
+            mod._lib = None
+            mod.load_library(str(tmp_path / "missing.so"))
+        finally:
+            mod._lib = saved

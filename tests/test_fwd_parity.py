@@ -1,0 +1,129 @@
+"""Forward parity: CUDA library (through the C ABI) vs the fp64 oracle.
+
+Small and medium shapes are compared element by element over the whole
+output (several tiles, ragged tails, GQA groups, causal and not).  The five
+named workloads are compared on seeded sampled rows at full size, in the
+launch configuration the benchmark times.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import exact_attention_95_gb300 as pkg
+from exact_attention_95_gb300 import inputs
+
+from parity import (F32_TOL, LSE_TOL, O_TOL, check_o, f64, make, to_dev)
+
+pytestmark = pytest.mark.gpu
+
+
+def _run(B, Hq, Hkv, N, d, causal, seed, out_dtype=torch.float32, q_mul=1.0, scale=None):
+    t = make(B, Hq, Hkv, N, d, seed, q_mul=q_mul, names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    scale = 1.0 / np.sqrt(d) if scale is None else scale
+    O, L = pkg.attn_fwd(g["Q"], g["K"], g["V"], scale, causal, out_dtype=out_dtype)
+    torch.cuda.synchronize()
+    assert pkg.attn_last_device_status() == pkg.ATTN_OK
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    Oref, Lref = oracle.fwd(f["Q"], f["K"], f["V"], scale, causal)
+    return f64(O), f64(L), Oref, Lref
+
+
+SHAPES = [
+    # B, Hq, Hkv, N, d
+    (1, 1, 1, 1, 64),
+    (1, 2, 1, 3, 128),
+    (2, 2, 2, 127, 64),
+    (1, 4, 2, 128, 128),
+    (1, 2, 1, 129, 64),
+    (2, 4, 1, 255, 128),
+    (1, 8, 2, 300, 64),
+    (1, 2, 2, 640, 128),
+    (1, 4, 4, 1000, 128),
+]
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("shape", SHAPES, ids=lambda s: "B%dHq%dHkv%dN%dd%d" % s)
+def test_fwd_full_parity_f32_out(shape, causal):
+    B, Hq, Hkv, N, d = shape
+    O, L, Oref, Lref = _run(B, Hq, Hkv, N, d, causal, seed=1000 + N + d)
+    err_o, ok = check_o(O, Oref, bf16_out=False)
+    err_l = np.abs(L - Lref).max()
+    assert ok, f"O max-abs {err_o:.3e}"
+    assert err_l <= LSE_TOL, f"LSE max-abs {err_l:.3e}"
+    # Error budget of bf16 P with fp32 accumulation: far below the bar on average.
+    assert np.sqrt(np.mean((O - Oref) ** 2)) < 2e-3
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_bf16_out_and_large_logits(causal):
+    # Q x8 gives logit std ~8 (the large-logit stress of the causal d=128 workload).
+    O, L, Oref, Lref = _run(1, 4, 2, 700, 128, causal, seed=77, out_dtype=torch.bfloat16, q_mul=8.0)
+    err_o, ok = check_o(O, Oref, bf16_out=True)
+    assert ok, f"O max-abs {err_o:.3e}"
+    assert np.abs(L - Lref).max() <= LSE_TOL
+
+
+def test_fwd_is_deterministic():
+    t = make(1, 4, 2, 513, 128, 5, names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    a = pkg.attn_fwd(g["Q"], g["K"], g["V"], 0.1, True)
+    b = pkg.attn_fwd(g["Q"], g["K"], g["V"], 0.1, True)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("N,causal", [(256, False), (200, True), (33, False)])
+def test_fwd_f32_path(N, causal):
+    t = make(1, 2, 1, N, 64, 2024 + N, dtype="f32", names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    O, L = pkg.attn_fwd(g["Q"], g["K"], g["V"], 0.125, causal)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    Oref, Lref = oracle.fwd(f["Q"], f["K"], f["V"], 0.125, causal)
+    assert np.abs(f64(O) - Oref).max() <= F32_TOL
+    assert np.abs(f64(L) - Lref).max() <= F32_TOL
+
+
+def test_fwd_f32_toy_row():
+    # The 3-key toy row of the worked example on the fp32 path (d=64, zero padded):
+    # q = e_0, k_j = s_j e_0, v_j = (1, 0, 1)_j e_0, scale = 1 -> O_0 = 0.7517...
+    Q = torch.zeros(1, 1, 3, 64, device="cuda")
+    K = torch.zeros(1, 1, 3, 64, device="cuda")
+    V = torch.zeros(1, 1, 3, 64, device="cuda")
+    Q[0, 0, :, 0] = 1.0
+    K[0, 0, :, 0] = torch.tensor([1.414, 0.707, 0.707])
+    V[0, 0, :, 0] = torch.tensor([1.0, 0.0, 1.0])
+    O, L = pkg.attn_fwd(Q, K, V, 1.0, False)
+    Oref, Lref = oracle.fwd(Q.double().cpu().numpy(), K.double().cpu().numpy(),
+                            V.double().cpu().numpy(), 1.0, False)
+    assert np.abs(f64(O) - Oref).max() <= F32_TOL
+    assert abs(float(O[0, 0, 0, 0]) - 0.752) < 5e-4
+
+
+@pytest.mark.parametrize("name", ["c1", "c2", "c3", "c4", "c5"])
+def test_fwd_workload_sampled_rows(name):
+    """Full-size workload, bench launch configuration, 512 seeded sampled rows."""
+    w = inputs.WORKLOADS[name]
+    t = inputs.workload_tensors(w, names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    O, L = pkg.attn_fwd(g["Q"], g["K"], g["V"], w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert pkg.attn_last_device_status() == pkg.ATTN_OK
+    total = w.B * w.Hq * w.N
+    rows = inputs.sample_rows(0xABC0 + w.config_id, total, 512,
+                              must=[0, 1, 127, 128, w.N - 1, total - 1])
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    Oref, Lref = oracle.fwd_rows(f["Q"], f["K"], f["V"], w.scale, w.causal, rows)
+    Og = f64(O.reshape(-1, w.d)[torch.from_numpy(rows).to(O.device)])
+    Lg = f64(L.reshape(-1)[torch.from_numpy(rows).to(L.device)])
+    if w.dtype == "f32":
+        assert np.abs(Og - Oref).max() <= F32_TOL
+        assert np.abs(Lg - Lref).max() <= F32_TOL
+    else:
+        err, ok = check_o(Og, Oref, bf16_out=True)
+        assert ok, f"O max-abs {err:.3e}"
+        assert np.abs(Lg - Lref).max() <= LSE_TOL
+    # Properties that hold at any size, over the whole output.
+    assert torch.isfinite(O).all() and torch.isfinite(L).all()
