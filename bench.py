@@ -1,0 +1,454 @@
+#!/usr/bin/env python
+"""Benchmark: exact attention forward + backward on GB300.
+
+One step = one pass of the whole path on one batch of synthetic input:
+attn_fwd, then the backward (preprocess, main, dQ convert) through the C ABI.
+The workload is the causal d=128 N=4096 bf16 configuration (B=2, H=32, Q
+scaled by 8).  FLOPs follow the usual convention: forward 4*N^2*d*H*B, halved
+for causal; backward 2.5x forward.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 it runs under torch.distributed (one process per GPU, NCCL); every
+rank processes its own copy of the batch (weak scaling, no data exchange) and
+the time is the maximum over ranks.  ``--impl reference`` times the fp64 CPU
+oracle on the host cores on a bounded sample of the same workload.
+
+Rank 0 prints one JSON line.
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "attention fwd/bwd TFLOPS (bf16, causal, N=4K, d=128) and % of GB300 tensor peak"
+WORKLOAD = "c3"
+FALLBACK_PEAK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
+L2_BYTES = 126 * 1024 * 1024
+
+
+def parse_args(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    return ap.parse_args(argv)
+
+
+# ---------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def init_dist(backend: str):
+    import torch.distributed as dist
+    rank, world, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return rank, world
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+def max_over_ranks(x: float, device=None) -> float:
+    """Maximum of a per-rank float over all ranks (the value itself at world 1)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def shard_units(n_units: int, rank: int, world: int):
+    """Contiguous, balanced split of n_units independent (batch, kv-head) units."""
+    base, extra = divmod(n_units, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
+# ---------------------------------------------------------------- peaks, clocks
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAK), "fallback"
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu):
+        self.gpu = gpu
+        self.proc = None
+        self.tmp = None
+
+    def __enter__(self):
+        self.tmp = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=self.tmp, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.send_signal(signal.SIGTERM)
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        self.tmp.close()
+
+    def summary(self):
+        rows = []
+        try:
+            with open(self.tmp.name) as f:
+                for line in f:
+                    parts = [p.strip() for p in line.split(",")]
+                    if len(parts) < 7:
+                        continue
+                    try:
+                        rows.append((float(parts[0]), float(parts[1]), parts[3:7]))
+                    except ValueError:
+                        continue
+        finally:
+            os.unlink(self.tmp.name)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, r in rows for i in range(4) if r[i].lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows), "sm_max_mhz": max(r[1] for r in rows),
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ---------------------------------------------------------------- oracle timing
+def oracle_step(w, t64, n_tokens: int, head: int):
+    """fp64 oracle forward + backward on the causal prefix [0, n_tokens) of one
+    head of the workload; returns (seconds, convention FLOPs credited)."""
+    import numpy as np
+    import oracle
+    b, h = divmod(head % (w.B * w.Hq), w.Hq)
+    hk = h // (w.Hq // w.Hkv)
+    sl = slice(0, n_tokens)
+    Q = np.ascontiguousarray(t64["Q"][b:b + 1, h:h + 1, sl])
+    K = np.ascontiguousarray(t64["K"][b:b + 1, hk:hk + 1, sl])
+    V = np.ascontiguousarray(t64["V"][b:b + 1, hk:hk + 1, sl])
+    dO = np.ascontiguousarray(t64["dO"][b:b + 1, h:h + 1, sl])
+    t0 = time.perf_counter()
+    oracle.fwd(Q, K, V, w.scale, w.causal)
+    oracle.bwd(Q, K, V, dO, w.scale, w.causal)
+    dt = time.perf_counter() - t0
+    f = 4.0 * n_tokens * n_tokens * w.d / (2 if w.causal else 1)
+    return dt, 3.5 * f
+
+
+def oracle_tensors(w):
+    from exact_attention_95_gb300 import inputs
+    # Only batch 0 is sampled; generate the needed prefix of each tensor.
+    t = inputs.workload_tensors(w)
+    return {k: inputs.to_f64(v[:1]) for k, v in t.items()}
+
+
+def size_oracle_sample(w, t64, budget_s: float) -> int:
+    """Prefix length whose oracle step takes about budget_s (cost ~ n^2)."""
+    n0 = 512
+    dt, _ = oracle_step(w, t64, n0, 0)
+    n = int(n0 * math.sqrt(max(budget_s, 1e-3) / max(dt, 1e-6)))
+    return max(64, min(w.N, n // 64 * 64))
+
+
+def cpu_cores():
+    return os.cpu_count() or 1
+
+
+# ---------------------------------------------------------------- reference arm
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    from exact_attention_95_gb300 import inputs
+    w = inputs.WORKLOADS[WORKLOAD]
+    t64 = oracle_tensors(w)
+    steps, warm = max(1, args.steps), max(0, args.warmup)
+    per_step = min(30.0, 150.0 / (steps + warm))
+    n = size_oracle_sample(w, t64, per_step)
+    for i in range(warm):
+        oracle_step(w, t64, n, i)
+    tot_t = tot_f = 0.0
+    for i in range(steps):
+        dt, fl = oracle_step(w, t64, n, warm + i)
+        tot_t += dt
+        tot_f += fl
+    value = tot_f / tot_t / 1e12
+    sample = (f"fp64 oracle forward+backward of the causal prefix of {n} tokens of one head "
+              f"per step (head index = step), from the {WORKLOAD} workload tensors")
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
+        "warmup": warm, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": workload_config(w), "impl": "reference",
+        "cpu_baseline": {"value": value, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+                         "sample": sample},
+        "e2e": {"value": value, "unit": "TFLOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def workload_config(w):
+    return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
+            "causal": w.causal, "q_scale": w.q_mul, "scale": w.scale,
+            "l2": "inputs larger than L2 (Q,K,V,dO,O 64 MiB each + 128 MiB dQ accumulator "
+                  "vs 126 MiB L2); no flush"}
+
+
+# ---------------------------------------------------------------- native arm
+def run_native(args):
+    import numpy as np
+    import torch
+
+    rank, world = init_dist("nccl")
+    _, _, local = dist_env()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    import exact_attention_95_gb300 as pkg
+    from exact_attention_95_gb300 import inputs
+
+    pkg.load_library()
+    w = inputs.WORKLOADS[WORKLOAD]
+    t_np = inputs.workload_tensors(w)
+
+    def dev_bf16(a):
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+
+    Q, K, V, dO = (dev_bf16(t_np[k]) for k in ("Q", "K", "V", "dO"))
+    O = torch.empty_like(Q)
+    LSE = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    dQ, dK, dV = torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)
+    ws = torch.empty(pkg.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+    stream = torch.cuda.current_stream()
+    scale, causal = w.scale, w.causal
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pkg.attn_fwd(Q, K, V, scale, causal, O=O, LSE=LSE, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+        pkg.attn_bwd(Q, K, V, O, dO, LSE, scale, causal, dQ, dK, dV, ws, stream, stage="preprocess")
+        if ev is not None:
+            ev[2].record(stream)
+        pkg.attn_bwd(Q, K, V, O, dO, LSE, scale, causal, dQ, dK, dV, ws, stream, stage="main")
+        if ev is not None:
+            ev[3].record(stream)
+        pkg.attn_bwd(Q, K, V, O, dO, LSE, scale, causal, dQ, dK, dV, ws, stream, stage="convert")
+        if ev is not None:
+            ev[4].record(stream)
+
+    launches_per_step = 4
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pkg.attn_last_device_status() != pkg.ATTN_OK:
+        raise RuntimeError("device status not OK after warm-up")
+
+    K_steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K_steps)]
+    barrier()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(local)
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        for i in range(K_steps):
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier()
+    st = pkg.attn_last_device_status()
+    if st != pkg.ATTN_OK:
+        raise RuntimeError(f"device status {pkg.attn_status_string(st)} in the timed region")
+    total_ms = evs[0][0].elapsed_time(evs[-1][4])
+    fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    main_ms = [e[2].elapsed_time(e[3]) for e in evs]
+    cv_ms = [e[3].elapsed_time(e[4]) for e in evs]
+    total_ms = max_over_ranks(total_ms, dev)
+    clocks = clk.summary()
+
+    ffl, bfl = w.fwd_flops(), w.bwd_flops()
+    ms_step = total_ms / K_steps
+    value = (ffl + bfl) * world / (total_ms / 1e3 / K_steps) / 1e12 / 1.0
+    peaks, peak_src = load_peaks()
+    burst = float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
+    fwd_avg = statistics.mean(fwd_ms)
+    main_avg = statistics.mean(main_ms)
+    fwd_tf = ffl / (fwd_avg / 1e3) / 1e12
+    bwd_avg = statistics.mean(p + m + c for p, m, c in zip(pre_ms, main_ms, cv_ms))
+    bwd_tf = bfl / (bwd_avg / 1e3) / 1e12
+    main_tf = bfl / (main_avg / 1e3) / 1e12
+    if main_avg >= fwd_avg:
+        dom, dom_tf = "bwd_main_kernel (attn_bwd_main)", main_tf
+    else:
+        dom, dom_tf = "fwd_bf16_kernel (attn_fwd)", fwd_tf
+    traffic = load_traffic(dom)
+    roofline = {"bound": "tensor", "achieved": dom_tf, "peak": sustained, "unit": "TFLOP/s",
+                "frac": dom_tf / sustained, "traffic": traffic, "kernel": dom,
+                "peak_source": f"bf16_tflops_sustained of {peak_src}"}
+
+    e2e = run_e2e(args, pkg, w, t_np, dev, stream, ffl + bfl, world)
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K_steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded iid N(0,1), bf16)",
+        "config": dict(workload_config(w), parallelism=f"replicas x{world} (weak)"),
+        "fwd": {"ms": fwd_avg, "tflops": fwd_tf, "pct_of_burst_peak": 100 * fwd_tf / burst,
+                "pct_of_nominal_2250": 100 * fwd_tf / 2250.0},
+        "bwd": {"ms": bwd_avg, "tflops": bwd_tf, "pct_of_burst_peak": 100 * bwd_tf / burst,
+                "pct_of_nominal_2250": 100 * bwd_tf / 2250.0,
+                "ms_preprocess": statistics.mean(pre_ms), "ms_main": main_avg,
+                "ms_convert": statistics.mean(cv_ms)},
+        "roofline": roofline,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K_steps,
+        "clocks": clocks,
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def load_traffic(kernel_desc):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu summary."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except (OSError, ValueError):
+        return None
+    key = "bwd_main" if kernel_desc.startswith("bwd_main") else "fwd"
+    ent = d.get(key)
+    if not ent or ent.get("stale"):
+        return None
+    return ent.get("bytes_per_launch")
+
+
+def run_e2e(args, pkg, w, t_np, dev, stream, flops, world):
+    """Same step through the public API with pinned host buffers: H2D of the
+    inputs and D2H of O, dQ, dK, dV inside the timed region."""
+    import numpy as np
+    import torch
+
+    host = {k: torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).pin_memory()
+            for k in ("Q", "K", "V", "dO")}
+    dbuf = {k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in host.items()}
+    out_shapes = {"O": host["Q"].shape, "dQ": host["Q"].shape, "dK": host["K"].shape,
+                  "dV": host["V"].shape}
+    hout = {k: torch.empty(s, dtype=torch.bfloat16).pin_memory() for k, s in out_shapes.items()}
+    LSE = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
+                     device=dev)
+
+    def step():
+        for k in dbuf:
+            dbuf[k].copy_(host[k], non_blocking=True)
+        O, L = pkg.attn_fwd(dbuf["Q"], dbuf["K"], dbuf["V"], w.scale, w.causal, LSE=LSE,
+                            stream=stream)
+        dQ, dK, dV = pkg.attn_bwd(dbuf["Q"], dbuf["K"], dbuf["V"], O, dbuf["dO"], L, w.scale,
+                                  w.causal, workspace=ws, stream=stream)
+        for k, t in (("O", O), ("dQ", dQ), ("dK", dK), ("dV", dV)):
+            hout[k].copy_(t, non_blocking=True)
+
+    for _ in range(2):
+        step()
+    torch.cuda.synchronize()
+    n = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(n):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(e0.elapsed_time(e1), dev) / n
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = sum(t.numel() * t.element_size() for t in hout.values())
+    return {"value": flops * world / (ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+
+
+def cpu_baseline(w, budget_s):
+    t64 = oracle_tensors(w)
+    tot_t = tot_f = 0.0
+    heads = 0
+    n = w.N
+    # Full heads while they fit the budget; otherwise a shorter causal prefix.
+    dt0, fl0 = oracle_step(w, t64, 512, 0)
+    est_full = dt0 * (w.N / 512) ** 2
+    if est_full > budget_s:
+        n = size_oracle_sample(w, t64, budget_s)
+    while tot_t < budget_s and heads < w.Hq:
+        dt, fl = oracle_step(w, t64, n, heads)
+        tot_t += dt
+        tot_f += fl
+        heads += 1
+    return {"value": tot_f / tot_t / 1e12, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
+            "sample": f"fp64 oracle forward+backward of {heads} head(s) of batch 0 of {WORKLOAD}, "
+                      f"causal prefix of {n} tokens each, {tot_t:.1f} s"}
+
+
+def main(argv=None):
+    args = parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_native(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

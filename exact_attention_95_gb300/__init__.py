@@ -34,8 +34,11 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5
 ATTN_BF16, ATTN_F32 = 0, 1
 
-EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_workspace_size", "attn_status_string",
-            "attn_last_device_status", "attn_selftest_wait_timeout")
+EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_convert",
+            "attn_bwd_workspace_size", "attn_status_string", "attn_last_device_status",
+            "attn_selftest_wait_timeout")
+_BWD_STAGES = {"all": "attn_bwd", "preprocess": "attn_bwd_preprocess", "main": "attn_bwd_main",
+               "convert": "attn_bwd_convert"}
 
 _lock = threading.Lock()
 _lib = None
@@ -61,9 +64,11 @@ def load_library(path: str = LIB_PATH):
         vp, i32, f32, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
         lib.attn_fwd.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, i32, vp]
         lib.attn_fwd.restype = i32
-        lib.attn_bwd.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
-                                 i32, i32, vp, sz, vp]
-        lib.attn_bwd.restype = i32
+        for fname in _BWD_STAGES.values():
+            fn = getattr(lib, fname)
+            fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
+                           i32, i32, vp, sz, vp]
+            fn.restype = i32
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i32]
@@ -143,8 +148,12 @@ def attn_fwd(Q, K, V, scale=None, causal=False, out_dtype=None, O=None, LSE=None
 
 
 def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV=None,
-             workspace=None, stream=None):
-    """dQ, dK, dV of O = attention(Q, K, V) given dO and the forward's LSE."""
+             workspace=None, stream=None, stage="all"):
+    """dQ, dK, dV of O = attention(Q, K, V) given dO and the forward's LSE.
+
+    ``stage`` selects one of the C entry points: "all" (attn_bwd) or one of
+    "preprocess", "main", "convert" (run in that order with the same
+    workspace to obtain the same result)."""
     lib = load_library()
     B, Hq, N, d = Q.shape
     Hkv = K.shape[1]
@@ -163,10 +172,11 @@ def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV
     ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d)
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
-    rc = lib.attn_bwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
-                      _ptr(dV), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), ATTN_BF16,
-                      _ptr(workspace), workspace.numel() * workspace.element_size(),
-                      _stream(stream))
+    fname = _BWD_STAGES[stage]
+    rc = getattr(lib, fname)(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                             _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, float(scale),
+                             int(bool(causal)), ATTN_BF16, _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream))
     if rc != ATTN_OK:
-        raise AttnError(rc, "attn_bwd")
+        raise AttnError(rc, fname)
     return dQ, dK, dV

@@ -166,10 +166,14 @@ size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {
   return bwd_workspace_bytes(B, Hq, N, d);
 }
 
-attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
-                     const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
-                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                     attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void* V,
+                       const void* O, const void* dO, const float* LSE, void* dQ, void* dK,
+                       void* dV, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                       attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
@@ -215,9 +219,47 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal;
   p.wait_limit_ns = wait_limit();
-  cudaError_t e = launch_bwd_bf16(d, tq, tk, tv, tdo, p, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_bwd_bf16(d, tq, tk, tv, tdo, p, stages, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
+                     const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                     int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                     attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_stages(kBwdAll, Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal,
+                    dtype, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_preprocess(const void* Q, const void* K, const void* V, const void* O,
+                                const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                                attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                void* stream) {
+  return bwd_stages(kBwdPre, Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal,
+                    dtype, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                          int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                          attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  return bwd_stages(kBwdMain, Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal,
+                    dtype, workspace, workspace_bytes, stream);
+}
+
+attn_status attn_bwd_convert(const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                             attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                             void* stream) {
+  return bwd_stages(kBwdConvert, Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal,
+                    dtype, workspace, workspace_bytes, stream);
 }
 
 attn_status attn_last_device_status(void* stream) {

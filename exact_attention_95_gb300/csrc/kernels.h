@@ -55,8 +55,11 @@ struct BwdParams {
 // Workspace layout of the backward (bytes), all fp32: dQacc then D then LSE2.
 size_t bwd_workspace_bytes(int B, int Hq, int N, int d);
 
+// Stages of the backward, launched in this order.
+enum : unsigned { kBwdPre = 1u, kBwdMain = 2u, kBwdConvert = 4u, kBwdAll = 7u };
+
 cudaError_t launch_bwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const CUtensorMap& tmdO,
-                            const BwdParams& p, cudaStream_t stream);
+                            const BwdParams& p, unsigned stages, cudaStream_t stream);
 
 }  // namespace attn

@@ -99,6 +99,30 @@ attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                      attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The three stages attn_bwd runs, in this order, as separate calls with the
+ * same arguments (for callers that schedule or time them separately):
+ *   attn_bwd_preprocess  D = rowsum(dO * O), LSE in log2 units, zeroed dQ
+ *                        accumulator (all in the workspace);
+ *   attn_bwd_main        the recompute-based tile loop: dK, dV written, dQ
+ *                        accumulated in the workspace;
+ *   attn_bwd_convert     dQ = bf16(scale * accumulator).
+ * Each stage reads what the previous ones wrote to the workspace; running
+ * them in order on one stream equals one attn_bwd call. */
+attn_status attn_bwd_preprocess(const void* Q, const void* K, const void* V, const void* O,
+                                const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                                int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                                attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                                void* stream);
+attn_status attn_bwd_main(const void* Q, const void* K, const void* V, const void* O,
+                          const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                          int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                          attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream);
+attn_status attn_bwd_convert(const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                             attn_dtype dtype, void* workspace, size_t workspace_bytes,
+                             void* stream);
+
 /* Bytes of workspace attn_bwd needs: an fp32 dQ accumulator and two fp32
  * per-row vectors (D = rowsum(dO * O) and LSE in log2 units).  0 on bad sizes. */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
