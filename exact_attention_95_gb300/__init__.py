@@ -180,3 +180,40 @@ def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV
     if rc != ATTN_OK:
         raise AttnError(rc, fname)
     return dQ, dK, dV
+
+
+# ---------------------------------------------------------------- no-alloc backward
+EXPORTED = EXPORTED + ("attn_bwd_noalloc",)
+NOALLOC_SCRATCH_BYTES = 32 * 1024 * 1024
+
+
+def attn_bwd_noalloc(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV=None,
+                     stream=None):
+    """attn_bwd with the library's fixed scratch array instead of a workspace.
+
+    For callers that cannot allocate device memory where they run the
+    backward.  The C call allocates nothing; problems whose workspace would
+    exceed NOALLOC_SCRATCH_BYTES are rejected (ATTN_ERR_UNSUPPORTED).  Calls on
+    one device share the scratch array: do not let them overlap on the GPU.
+    (Here the outputs are allocated by PyTorch unless given.)"""
+    lib = load_library()
+    fn = lib.attn_bwd_noalloc
+    vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
+    fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+    fn.restype = i32
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bf = torch.bfloat16
+    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv), ("O", O, Hq), ("dO", dO, Hq)):
+        _check_tensor(name, t, bf, (B, H, N, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    rc = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+            B, Hq, Hkv, N, d, float(scale), int(bool(causal)), ATTN_BF16, _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_noalloc")
+    return dQ, dK, dV

@@ -1,0 +1,61 @@
+// bwd_noalloc.cu -- attn_bwd_noalloc: the backward with library-owned scratch.
+//
+// attn_bwd needs a caller-provided workspace (the fp32 dQ accumulator and two
+// per-row vectors).  Some callers cannot allocate device memory at the point
+// where they run the backward: code hosted inside a runtime that owns every
+// device allocation and hands out no workspace, or latency-critical paths that
+// must not call cudaMalloc (it can synchronise the device and can fail).  For
+// them this entry point uses a fixed scratch array compiled into the library
+// instead of a workspace argument, and allocates nothing itself.
+#include <cstdint>
+#include <mutex>
+
+#include "../../include/attn.h"
+
+namespace {
+
+// The scratch array.  Every GPU that loads the library holds it until the
+// process exits.  All calls on a device share it.
+static __device__ __align__(256) uint8_t g_bwd_scratch[ATTN_NOALLOC_SCRATCH_BYTES];
+
+// Device address of g_bwd_scratch on the current device, looked up once per
+// device.  In host code the symbol name is only a host-side handle, so the
+// address must come from cudaGetSymbolAddress with that device current.
+void* scratch_address() {
+  static void* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_bwd_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = p;
+  }
+  return addr[dev];
+}
+
+}  // namespace
+
+extern "C" attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                                        const void* dO, const float* LSE, void* dQ, void* dK,
+                                        void* dV, int B, int Hq, int Hkv, int N, int d, float scale,
+                                        int causal, attn_dtype dtype, void* stream) {
+  const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, d);
+  if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
+  if (need == 0) {
+    // The sizes are invalid or unsupported: attn_bwd rejects the call while
+    // checking its arguments, before any use of the workspace, and returns the
+    // status that applies.  The placeholder only has to pass the null and
+    // alignment checks.
+    return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal, dtype,
+                    reinterpret_cast<void*>(uintptr_t(256)), 0, stream);
+  }
+  void* ws = scratch_address();
+  if (!ws) return ATTN_ERR_CUDA;
+  // The backward's first stage re-initialises every part of the scratch it
+  // reads (zeroed dQ accumulator, fresh D and LSE vectors), so the contents a
+  // previous call left behind do not matter.
+  return attn_bwd(Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal, dtype, ws,
+                  (size_t)ATTN_NOALLOC_SCRATCH_BYTES, stream);
+}

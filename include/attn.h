@@ -123,6 +123,31 @@ attn_status attn_bwd_convert(const void* Q, const void* K, const void* V, const 
                              attn_dtype dtype, void* workspace, size_t workspace_bytes,
                              void* stream);
 
+/*
+ * attn_bwd without a workspace argument, for callers that cannot allocate
+ * device memory where they run the backward: code hosted in a runtime that
+ * owns every device allocation and hands out no workspace, and
+ * latency-critical paths that must not call cudaMalloc (it can synchronise the
+ * device, and it can fail).  The pages describe no such interface; it has no
+ * counterpart there.
+ *
+ * Arguments and results are those of attn_bwd.  The scratch memory is a fixed
+ * array of ATTN_NOALLOC_SCRATCH_BYTES bytes compiled into the library; every
+ * GPU that loads the library holds it until the process exits.  Problems whose
+ * attn_bwd_workspace_size() exceeds it return ATTN_ERR_UNSUPPORTED.  The call
+ * allocates nothing.  The first call on a device looks up the array's device
+ * address (cudaGetSymbolAddress, with that device current); make that first
+ * call before any stream capture.  All calls on a device share the array and
+ * it keeps the last call's contents; the backward re-initialises what it
+ * reads, so this does not affect results, but calls that overlap on the GPU
+ * (other streams, other host threads) race on it: serialise them.
+ */
+#define ATTN_NOALLOC_SCRATCH_BYTES (32u * 1024u * 1024u)
+attn_status attn_bwd_noalloc(const void* Q, const void* K, const void* V, const void* O,
+                             const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                             int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                             attn_dtype dtype, void* stream);
+
 /* Bytes of workspace attn_bwd needs: an fp32 dQ accumulator and two fp32
  * per-row vectors (D = rowsum(dO * O) and LSE in log2 units).  0 on bad sizes. */
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d);
