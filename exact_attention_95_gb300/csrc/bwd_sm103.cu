@@ -163,8 +163,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bhk = blockIdx.x;  // b * Hkv + hk
-  const int jt = blockIdx.y;   // key tile
+  // CTA -> (b * Hkv + hk, key tile): the key tiles of a few kv heads run together
+  // so that their query-side operands and dQ accumulator stay in L2; within a
+  // group, key tile 0 (the most query tiles when causal) comes first.
+  int bhk, jt;
+  grouped_order(blockIdx.x, p.B * p.Hkv, (p.N + kBK - 1) / kBK, p.head_group, bhk, jt);
   const int k0 = jt * kBK;
   const int b = bhk / p.Hkv;
   const int hk = bhk - b * p.Hkv;
@@ -318,9 +321,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       const int g = t / per_head;
       const int it = i0 + (t - g * per_head);
       const int q0 = it * kBQ;
-      const uint8_t* stp = smem + C::OFF_STAGE + s * C::STAGE_BYTES;
-      const float* lse2 = reinterpret_cast<const float*>(stp + C::ST_LSE);
-      const float* dvec = reinterpret_cast<const float*>(stp + C::ST_D);
+      const uint32_t stp = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
       if (!mbar_wait(bar(C::B_STFULL + s), (t / C::STAGES) & 1, wc) ||
           !mbar_wait(bar(C::B_SFULL), t & 1, wc)) {
         ok = false;
@@ -336,10 +337,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       float pv[64];
       uint32_t pk[32];
 #pragma unroll
-      for (int c = 0; c < 64; ++c) {
-        float x = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -lse2[c]));
-        if (!key_ok || (diag && key > q0 + c)) x = 0.f;
-        pv[c] = x;
+      for (int c4 = 0; c4 < 16; ++c4) {
+        const float4 lq = lds_f4(stp + C::ST_LSE + 16 * c4);  // same address in every lane
+        const float l4[4] = {lq.x, lq.y, lq.z, lq.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int c = 4 * c4 + u;
+          float x = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -l4[u]));
+          if (!key_ok || (diag && key > q0 + c)) x = 0.f;
+          pv[c] = x;
+        }
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
@@ -353,17 +360,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         break;
       }
       tc_fence_after();
-      uint32_t dr[2][32];
-      tmem_ld32(tmem + lane_off + C::TM_DP, dr[0]);
-      tmem_ld32(tmem + lane_off + C::TM_DP + 32, dr[1]);
-      tmem_ld_wait(dr[0]);
-      reg_fence32(dr[1]);
+      // dS = P (dP - D), one half of the 64 query columns at a time.
 #pragma unroll
-      for (int c = 0; c < 32; ++c) {
-        const float a = pv[2 * c] * (__uint_as_float(dr[(2 * c) >> 5][(2 * c) & 31]) - dvec[2 * c]);
-        const float bb =
-            pv[2 * c + 1] * (__uint_as_float(dr[(2 * c + 1) >> 5][(2 * c + 1) & 31]) - dvec[2 * c + 1]);
-        pk[c] = pack_bf16(a, bb);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t dr[32];
+        tmem_ld32(tmem + lane_off + C::TM_DP + 32 * half, dr);
+        tmem_ld_wait(dr);
+#pragma unroll
+        for (int c4 = 0; c4 < 8; ++c4) {
+          const float4 dq = lds_f4(stp + C::ST_D + 128 * half + 16 * c4);
+          const int c = 32 * half + 4 * c4;
+          pk[16 * half + 2 * c4] = pack_bf16(pv[c] * (__uint_as_float(dr[4 * c4]) - dq.x),
+                                             pv[c + 1] * (__uint_as_float(dr[4 * c4 + 1]) - dq.y));
+          pk[16 * half + 2 * c4 + 1] = pack_bf16(pv[c + 2] * (__uint_as_float(dr[4 * c4 + 2]) - dq.z),
+                                                 pv[c + 3] * (__uint_as_float(dr[4 * c4 + 3]) - dq.w));
+        }
       }
       tmem_st32(tmem + lane_off + C::TM_DP, pk);
       // dS^T row into shared memory for the dQ product (128-byte swizzle: the
@@ -372,12 +383,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         ok = false;
         break;
       }
-      uint8_t* dsrow = smem + C::OFF_DS + kr * 128;
+      const uint32_t dsrow = sDS + kr * 128;
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint4 v = make_uint4(pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
-        *reinterpret_cast<uint4*>(dsrow + ((c ^ (kr & 7)) << 4)) = v;
-      }
+      for (int c = 0; c < 8; ++c)
+        sts_u4(dsrow + ((c ^ (kr & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
       tmem_st_wait();
       tc_fence_before();
@@ -469,7 +478,7 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
     auto kern = bwd_main_kernel<D>;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.B * p.Hkv, (p.N + kBK - 1) / kBK);
+    dim3 grid(p.B * p.Hkv * ((p.N + kBK - 1) / kBK));
     kern<<<grid, kMainThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmdO, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }

@@ -5,59 +5,74 @@
 // FlashAttention" §5: per K/V tile, m+ = max(m, m~), l+ = e^{m-m+} l + rowsum(P~),
 // O+ = e^{m-m+} O + P~ V.  As in FlashAttention-2 ("从Online-Softmax到
 // FlashAttention V1/V2/V3", 0x05), O stays unnormalised and 1/l is applied
-// once at the end; each CTA owns one 128-row query tile and loops over K/V
-// (Q outer loop), so CTAs never communicate.  Causal tiles above the diagonal
-// are never visited and only the diagonal tile is masked (0x09's three tile
+// once at the end; each CTA owns its query rows and loops over K/V (Q outer
+// loop), so CTAs never communicate.  Causal tiles above the diagonal are never
+// visited and only tiles that cross the diagonal are masked (0x09's three tile
 // cases).  GQA reads K/V head h / (Hq / Hkv) by indexing (0x09).
 //
-// Mapping to the hardware (one CTA, 6 warps):
-//   warp 0      TMA producer: Q tile once, then K_j, V_j through a STAGES-deep
-//               ring of shared-memory slots (mbarrier full/empty pairs).
+// The running max may lag behind the true max: softmax(s) = e^{s-m} / sum e^{s-m}
+// holds for any m (§5.1 of the same notes), so a row only moves its m (and
+// rescales l and its O row) when the new tile's max exceeds it by more than
+// 2^8; otherwise P~ = 2^{s - m} <= 256, which bf16 P and fp32 l, O hold as
+// well as values <= 1.
+//
+// Mapping to the hardware (one CTA = two 128-row query tiles, 12 warps):
+//   warp 0      TMA producer: both Q tiles once, then K_j, V_j through a
+//               STAGES-deep ring of shared-memory slots (full/empty mbarriers).
 //   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
-//               S_j = Q K_j^T  (SS MMA, M=128 N=128, into TMEM buffer j%2)
-//               O  += P_j V_j  (TS MMA, P read from TMEM, V from shared memory)
-//   warps 2..5  softmax: thread r owns query row r; it reads its S row from
-//               TMEM (32x32b loads), keeps m and l in registers in log2 units,
-//               writes P as packed bf16 over the first 64 columns of the same
-//               S buffer, rescales its O row in TMEM when the max moved, and
-//               finally writes O / l and LSE.
-// TMEM columns: [0,128) S/P buffer 0, [128,256) buffer 1, [256,256+d) O.
+//               S_t = Q_t K_j^T  (SS MMA, M=128 N=128, TMEM buffer t)
+//               O_t += P_t V_j   (TS MMA, P_t read from TMEM, V from smem)
+//   warps 4..7  softmax of query tile 0, warps 8..11 of tile 1: thread r owns
+//               row r; it reads S from TMEM (32x32b loads), keeps m and l in
+//               registers (log2 units), writes P as packed bf16 over the first
+//               64 columns of its S buffer, rescales its O row in TMEM when m
+//               moves, and finally writes O / l and LSE.
+// The two tiles ping-pong: while one warpgroup computes exponentials the
+// tensor pipe runs the other tile's P V and its next Q K^T.
+// TMEM columns: [0,128) S/P of tile 0, [128,256) of tile 1, then O_0, O_1.
+// Registers: warpgroup 0 gives registers to the two softmax warpgroups
+// (setmaxnreg), which hold a whole S row each.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kBM = 128;  // query rows per CTA
+constexpr int kBM = 128;  // query rows per tile (two tiles per CTA)
 constexpr int kBN = 128;  // keys per K/V tile
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+constexpr int kLaunchRegs = 168;  // per-thread registers of a 384-thread CTA (3 warps per SMSP)
+constexpr int kRegsLow = 72;      // warpgroup 0 after setmaxnreg.dec
+constexpr int kRegsHigh = 216;    // softmax warpgroups after setmaxnreg.inc
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
+constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
 
 template <int D>
 struct Fwd {
   static constexpr int CB = D / 64;              // 128-byte column blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;  // one 128-row x 64-col bf16 block
   static constexpr int TILE_BYTES = CB * BLOCK_BYTES;
-  static constexpr int STAGES = D == 128 ? 4 : 6;
-  static constexpr int OFF_Q = 0;
-  static constexpr int OFF_KV = TILE_BYTES;
+  static constexpr int STAGES = D == 128 ? 4 : 8;
+  static constexpr int OFF_Q = 0;                // two Q tiles
+  static constexpr int OFF_KV = 2 * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
-  // barrier indices
   static constexpr int B_QFULL = 0;
   static constexpr int B_KVFULL = 1;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2
   static constexpr int B_PFULL = B_SFULL + 2;         // 2
-  static constexpr int B_ODONE = B_PFULL + 2;
-  static constexpr int B_DRAIN = B_ODONE + 1;
+  static constexpr int B_ODONE = B_PFULL + 2;         // 2
+  static constexpr int B_DRAIN = B_ODONE + 2;
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + alignment slack
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t IDESC_O = idesc_bf16(kBM, D, false, true);
-  static constexpr uint32_t TM_S = 0;
-  static constexpr uint32_t TM_O = 256;
+  static constexpr uint32_t TM_S = 0;    // + 128 * t
+  static constexpr uint32_t TM_O = 256;  // + D * t
 };
 
 template <int D>
@@ -77,14 +92,16 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  const int bh = blockIdx.x;                      // b * Hq + h
-  const int tile = p.n_qtiles - 1 - (int)blockIdx.y;  // heaviest causal tiles launch first
-  const int q0 = tile * kBM;
+  // CTA -> (b*Hq + h, pair of query tiles), heaviest pairs first within groups of heads.
+  int bh, rank;
+  grouped_order(blockIdx.x, p.B * p.Hq, p.n_pairs, p.head_group, bh, rank);
+  const int pair = p.n_pairs - 1 - rank;
+  const int q0 = pair * 2 * kBM;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
   int n_kv = (p.N + kBN - 1) / kBN;
-  if (p.causal) n_kv = min(n_kv, tile + 1);  // tiles right of the diagonal are skipped
+  if (p.causal) n_kv = min(n_kv, 2 * pair + 2);  // K/V tiles right of the diagonal are skipped
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
@@ -95,8 +112,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::B_SFULL + i), 1);
       mbar_init(bar(C::B_PFULL + i), kBM);
+      mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_ODONE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -111,15 +128,18 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    regs_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(C::B_QFULL), C::TILE_BYTES);
-      for (int cb = 0; cb < C::CB; ++cb)
-        tma_load_3d(sQ + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64, q0, bh);
+      mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
+      for (int t = 0; t < 2; ++t)
+        for (int cb = 0; cb < C::CB; ++cb)
+          tma_load_3d(sQ + t * C::TILE_BYTES + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64,
+                      q0 + t * kBM, bh);
       int li = 0;
       bool ok = true;
       for (int j = 0; j < n_kv && ok; ++j) {
@@ -141,76 +161,97 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
+    } else if (warp == 1 && lane == 0) {
+      // ---------------------------------------------------------- MMA issuer
       bool ok = mbar_wait(bar(C::B_QFULL), 0, wc);
       tc_fence_after();
-      auto issue_s = [&](int jj) -> bool {
-        const int li = 2 * jj;
-        const int s = li % C::STAGES;
-        if (!mbar_wait(bar(C::B_KVFULL + s), (li / C::STAGES) & 1, wc)) return false;
+      auto kv_slot = [&](int li) -> int { return li % C::STAGES; };
+      auto wait_kv = [&](int li) -> bool {
+        if (!mbar_wait(bar(C::B_KVFULL + kv_slot(li)), (li / C::STAGES) & 1, wc)) return false;
         tc_fence_after();
-        const uint32_t d_t = tmem + C::TM_S + (jj & 1) * 128;
-        const uint32_t kb = sKV + s * C::TILE_BYTES;
+        return true;
+      };
+      // S_t = Q_t K^T into buffer t.
+      auto issue_s = [&](int t, int li) {
+        const uint32_t kb = sKV + kv_slot(li) * C::TILE_BYTES;
+        const uint32_t qb = sQ + t * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          mma_ss(d_t, sdesc_sw128(sQ + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024), C::IDESC_S,
-                 kk > 0);
+          mma_ss(tmem + C::TM_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
+                 sdesc_sw128(kb + off, 16, 1024), C::IDESC_S, kk > 0);
         }
-        tc_commit(bar(C::B_SFULL + (jj & 1)));
-        tc_commit(bar(C::B_KVEMPTY + s));
-        return true;
+        tc_commit(bar(C::B_SFULL + t));
       };
-      if (ok) ok = issue_s(0);
-      for (int jj = 0; jj < n_kv && ok; ++jj) {
-        if (jj + 1 < n_kv) {
-          // S buffer (jj+1)&1 held P_{jj-1}; PV_{jj-1} must have consumed it.
-          if (jj >= 1 && !mbar_wait(bar(C::B_ODONE), (jj - 1) & 1, wc)) break;
-          if (!issue_s(jj + 1)) break;
-        }
-        if (!mbar_wait(bar(C::B_PFULL + (jj & 1)), (jj >> 1) & 1, wc)) break;
-        tc_fence_after();
-        const int li = 2 * jj + 1;
-        const int s = li % C::STAGES;
-        if (!mbar_wait(bar(C::B_KVFULL + s), (li / C::STAGES) & 1, wc)) break;
-        tc_fence_after();
-        const uint32_t vb = sKV + s * C::TILE_BYTES;
-        const uint32_t p_t = tmem + C::TM_S + (jj & 1) * 128;
+      // O_t += P_t V (A = 16 keys of P = 8 TMEM columns; B = 16 V rows, MN-major).
+      auto issue_pv = [&](int t, int li, bool acc) {
+        const uint32_t vb = sKV + kv_slot(li) * C::TILE_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < kBN / 16; ++kk) {
-          // A: 16 keys of P = 8 TMEM columns of packed bf16 pairs.
-          // B: V rows 16kk..16kk+15, MN-major (d contiguous), 2048 bytes per 16 rows.
-          mma_ts(tmem + C::TM_O, p_t + kk * 8, sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024),
-                 C::IDESC_O, (jj > 0 || kk > 0) ? 1u : 0u);
+        for (int kk = 0; kk < kBN / 16; ++kk)
+          mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_S + t * 128 + kk * 8,
+                 sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
+                 (acc || kk > 0) ? 1u : 0u);
+        tc_commit(bar(C::B_ODONE + t));
+      };
+      if (ok && (ok = wait_kv(0))) {
+        issue_s(0, 0);
+        issue_s(1, 0);
+        tc_commit(bar(C::B_KVEMPTY + kv_slot(0)));
+      }
+      for (int j = 0; j < n_kv && ok; ++j) {
+        const int liK = 2 * (j + 1), liV = 2 * j + 1;
+        const bool more = j + 1 < n_kv;
+        if (!wait_kv(liV)) break;
+        for (int t = 0; t < 2; ++t) {
+          if (!mbar_wait(bar(C::B_PFULL + t), j & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_pv(t, liV, j > 0);
+          if (t == 1) tc_commit(bar(C::B_KVEMPTY + kv_slot(liV)));
+          if (more) {
+            if (t == 0 && !wait_kv(liK)) {
+              ok = false;
+              break;
+            }
+            // S buffer t holds P_t of this tile until P_t V has completed.
+            if (!mbar_wait(bar(C::B_ODONE + t), j & 1, wc)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            issue_s(t, liK);
+            if (t == 1) tc_commit(bar(C::B_KVEMPTY + kv_slot(liK)));
+          }
         }
-        tc_commit(bar(C::B_ODONE));
-        tc_commit(bar(C::B_KVEMPTY + s));
       }
       // Drain: all MMAs of this thread complete before TMEM is released.
       tc_commit(bar(C::B_DRAIN));
       mbar_wait_drain(bar(C::B_DRAIN), 0, wc);
     }
   } else {
+    regs_inc<kRegsHigh>();
     // ------------------------------------------------------------ softmax
-    const int quad = warp & 3;  // TMEM lane quarter this warp may access
+    const int t = (warp - 4) >> 2;  // query tile of this warpgroup
+    const int quad = warp & 3;      // TMEM lane quarter this warp may access
     const int row = quad * 32 + lane;
-    const int q = q0 + row;
+    const int qt0 = q0 + t * kBM;
+    const int q = qt0 + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t s_t = tmem + lane_off + C::TM_S + t * 128;
+    const uint32_t o_t = tmem + lane_off + C::TM_O + t * D;
     const float sl2 = p.scale_log2;
-    float m = -INFINITY;  // running max of scale*s in log2 units
+    float m = -INFINITY;  // running (possibly stale) max of scale*s, log2 units
     float l = 0.f;        // running sum of 2^(scale*s*log2e - m)
     bool ok = true;
-    for (int jj = 0; jj < n_kv; ++jj) {
-      const int k0 = jj * kBN;
-      if (!mbar_wait(bar(C::B_SFULL + (jj & 1)), (jj >> 1) & 1, wc)) {
+    for (int j = 0; j < n_kv; ++j) {
+      const int k0 = j * kBN;
+      if (!mbar_wait(bar(C::B_SFULL + t), j & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      const uint32_t s_t = tmem + lane_off + C::TM_S + (jj & 1) * 128;
       uint32_t sr[4][32];
 #pragma unroll
       for (int c = 0; c < 4; ++c) tmem_ld32(s_t + c * 32, sr[c]);
@@ -218,9 +259,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr[1]);
       reg_fence32(sr[2]);
       reg_fence32(sr[3]);
-      // Mask: keys past N (ragged tail) and, on the diagonal tile, keys after q.
-      const bool need_mask = (k0 + kBN > p.N) || (p.causal && k0 + kBN - 1 > q0);
-      if (need_mask) {
+      // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
+      if ((k0 + kBN > p.N) || (p.causal && k0 + kBN - 1 > qt0)) {
         const int lim = p.causal ? min(p.N - 1, q) : p.N - 1;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
@@ -228,65 +268,64 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int i = 0; i < 32; ++i)
             if (k0 + c * 32 + i > lim) sr[c][i] = __float_as_uint(-INFINITY);
       }
-      float mx = -INFINITY;
+      float mp[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) mp[i] = -INFINITY;
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mx = fmaxf(mx, __uint_as_float(sr[c][i]));
-      const float m_new = fmaxf(m, mx * sl2);
-      const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-      const float alpha = ex2(m - m_use);  // 0 on the first tile (m = -inf)
-      float rs = 0.f;
-      uint32_t pk[4][16];
+        for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sr[c][i]));
+      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
+      // Move m only when the tile's max exceeds it by more than the threshold.
+      const bool move = mx > m + kRescaleThreshold;
+      float alpha = 1.f;
+      if (move) {
+        alpha = ex2(m - mx);  // 0 when m = -inf
+        m = mx;
+        l *= alpha;
+      }
+      const float m_use = (m == -INFINITY) ? 0.f : m;
+      if (j > 0 && __any_sync(0xffffffffu, move)) {
+        // O_t holds tiles < j (their P V completed before S_t of tile j was issued).
 #pragma unroll
-      for (int c = 0; c < 4; ++c)
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(o_t + c * 32, o);
+          tmem_ld_wait(o);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -m_use));
-          const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -m_use));
-          rs += p0 + p1;
-          pk[c][i] = pack_bf16(p0, p1);
+          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+          tmem_st32(o_t + c * 32, o);
         }
-      l = l * alpha + rs;
-      m = m_new;
-      if (jj > 0) {
-        // O holds the sum up to tile jj-1; wait for that PV before rescaling.
-        if (!mbar_wait(bar(C::B_ODONE), (jj - 1) & 1, wc)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+      }
+      float rs[8];
 #pragma unroll
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(tmem + lane_off + C::TM_O + c * 32, o);
-            tmem_ld_wait(o);
+      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      // P as packed bf16 pairs, stored in two halves of 32 TMEM columns: the
+      // first half lands on S columns [0, 32), already read into registers.
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(tmem + lane_off + C::TM_O + c * 32, o);
+      for (int half = 0; half < 2; ++half) {
+        uint32_t w[32];
+#pragma unroll
+        for (int cc = 0; cc < 2; ++cc) {
+          const int c = 2 * half + cc;
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -m_use));
+            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -m_use));
+            rs[i & 7] += p0 + p1;
+            w[cc * 16 + i] = pack_bf16(p0, p1);
           }
         }
+        tmem_st32(s_t + half * 32, w);
       }
-      // P (bf16) over the first 64 columns of this S buffer.
-      {
-        uint32_t w0[32], w1[32];
-#pragma unroll
-        for (int i = 0; i < 16; ++i) {
-          w0[i] = pk[0][i];
-          w0[16 + i] = pk[1][i];
-          w1[i] = pk[2][i];
-          w1[16 + i] = pk[3][i];
-        }
-        tmem_st32(s_t, w0);
-        tmem_st32(s_t + 32, w1);
-      }
+      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PFULL + (jj & 1)));
+      mbar_arrive(bar(C::B_PFULL + t));
     }
     // Epilogue: O / l and LSE.
-    if (ok && mbar_wait(bar(C::B_ODONE), (n_kv - 1) & 1, wc)) {
+    if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q < p.N;
@@ -294,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(tmem + lane_off + C::TM_O + c * 32, o);
+        tmem_ld32(o_t + c * 32, o);
         tmem_ld_wait(o);
         if (valid) {
           if (p.out_f32) {
@@ -338,9 +377,20 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
                    const FwdParams& p, cudaStream_t stream) {
   using C = Fwd<D>;
   auto kern = fwd_bf16_kernel<D>;
+  // setmaxnreg moves registers inside the launch allocation; refuse to launch
+  // if the compiler gave the kernel a different per-thread count than assumed
+  // (a larger split than the allocation would leave setmaxnreg.inc waiting).
+  static int regs = -1;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.Hq, p.n_qtiles);
+  dim3 grid(p.B * p.Hq * p.n_pairs);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }

@@ -14,6 +14,8 @@ struct FwdParams {
   int* status;      // device status word
   int B, Hq, Hkv, N;
   int n_qtiles;     // ceil(N / 128)
+  int n_pairs;      // ceil(n_qtiles / 2): each CTA owns two 128-row query tiles
+  int head_group;   // heads whose CTAs are launched together (L2 reuse of K/V)
   float scale_log2; // scale * log2(e)
   int causal;
   int out_f32;
@@ -49,6 +51,7 @@ struct BwdParams {
   float scale;          // softmax scale
   float scale_log2;     // scale * log2(e)
   int causal;
+  int head_group;       // kv heads whose CTAs are launched together (L2 reuse)
   unsigned long long wait_limit_ns;
 };
 

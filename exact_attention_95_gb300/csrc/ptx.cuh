@@ -256,3 +256,43 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 }
 
 }  // namespace attn
+
+namespace attn {
+
+// 16-byte shared-memory load/store through 32-bit shared addresses.
+__device__ __forceinline__ float4 lds_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared.v4.f32 {%0,%1,%2,%3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr));
+  return v;
+}
+__device__ __forceinline__ void sts_u4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+// Warpgroup register reallocation (all four warps of a warpgroup execute it).
+template <int N>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(N));
+}
+template <int N>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(N));
+}
+
+// Launch order of CTAs over (head, tile) pairs that keeps the tiles of a few
+// heads in flight together (so the operands they share stay in L2): CTAs come
+// in groups of `hg` heads; inside a group the tile rank varies slowest.
+__device__ __forceinline__ void grouped_order(int linear, int heads, int tiles, int hg, int& head,
+                                              int& rank) {
+  const int per_group = hg * tiles;
+  const int g = linear / per_group;
+  const int r = linear - g * per_group;
+  const int hg_here = min(hg, heads - g * hg);
+  rank = r / hg_here;
+  head = g * hg + (r - rank * hg_here);
+}
+
+}  // namespace attn
