@@ -248,64 +248,65 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      bool ok = mbar_wait(bar(C::B_KVFULL), 0, wc);
+    {
+      // The whole warp runs this loop (uniform operands); one elected lane issues.
+      bool ok = mbar_wait_warp(bar(C::B_KVFULL), 0, wc);
       for (int t = 0; t < T && ok; ++t) {
         const int s = t % C::STAGES;
         const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
-        if (!mbar_wait(bar(C::B_STFULL + s), (t / C::STAGES) & 1, wc)) break;
+        if (!mbar_wait_warp(bar(C::B_STFULL + s), (t / C::STAGES) & 1, wc)) break;
         // All MMAs of the previous iteration are complete: the S/P, dP/dS
         // TMEM regions and the dS shared-memory tile may be overwritten.
-        if (t > 0 && !mbar_wait(bar(C::B_MMADONE), (t - 1) & 1, wc)) break;
+        if (t > 0 && !mbar_wait_warp(bar(C::B_MMADONE), (t - 1) & 1, wc)) break;
         tc_fence_after();
         // S^T = K Q^T and dP^T = V dO^T (both K-major operands).
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * C::KBLK + (kk & 3) * 32;
           const uint32_t qa = (kk >> 2) * C::QBLK + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_S, sdesc_sw128(sK + ka, 16, 1024), sdesc_sw128(st + C::ST_Q + qa, 16, 1024),
+          mma_ss_warp(tmem + C::TM_S, sdesc_sw128(sK + ka, 16, 1024), sdesc_sw128(st + C::ST_Q + qa, 16, 1024),
                  C::IDESC_ST, kk > 0);
         }
-        tc_commit(bar(C::B_SFULL));
+        tc_commit_warp(bar(C::B_SFULL));
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t ka = (kk >> 2) * C::KBLK + (kk & 3) * 32;
           const uint32_t qa = (kk >> 2) * C::QBLK + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_DP, sdesc_sw128(sV + ka, 16, 1024),
+          mma_ss_warp(tmem + C::TM_DP, sdesc_sw128(sV + ka, 16, 1024),
                  sdesc_sw128(st + C::ST_DO + qa, 16, 1024), C::IDESC_ST, kk > 0);
         }
-        tc_commit(bar(C::B_DPFULL));
+        tc_commit_warp(bar(C::B_DPFULL));
         // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major: 16 query rows = 2048 bytes)
-        if (!mbar_wait(bar(C::B_PFULL), t & 1, wc)) break;
+        if (!mbar_wait_warp(bar(C::B_PFULL), t & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(tmem + C::TM_DV, tmem + C::TM_S + kk * 8,
+          mma_ts_warp(tmem + C::TM_DV, tmem + C::TM_S + kk * 8,
                  sdesc_sw128(st + C::ST_DO + kk * 2048, C::QBLK, 1024), C::IDESC_KV,
                  (t > 0 || kk > 0) ? 1u : 0u);
         // dK += dS^T Q
-        if (!mbar_wait(bar(C::B_DSFULL), t & 1, wc)) break;
+        if (!mbar_wait_warp(bar(C::B_DSFULL), t & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8,
+          mma_ts_warp(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8,
                  sdesc_sw128(st + C::ST_Q + kk * 2048, C::QBLK, 1024), C::IDESC_KV,
                  (t > 0 || kk > 0) ? 1u : 0u);
         // dQ^T = K^T dS^T  (A = K as MN-major [d x keys], B = dS^T MN-major [keys x queries]).
         // For d = 64 the instruction still has M = 128; lanes 64..127 read the
         // V tile as filler and are ignored.
-        if (t > 0 && !mbar_wait(bar(C::B_DQFREE), (t - 1) & 1, wc)) break;
+        if (t > 0 && !mbar_wait_warp(bar(C::B_DQFREE), (t - 1) & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_ss(tmem + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KBLK, 1024),
+          mma_ss_warp(tmem + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KBLK, 1024),
                  sdesc_sw128(sDS + kk * 2048, 8192, 1024), C::IDESC_DQ, kk > 0);
-        tc_commit(bar(C::B_DQFULL));
-        tc_commit(bar(C::B_STEMPTY + s));
-        tc_commit(bar(C::B_MMADONE));
+        tc_commit_warp(bar(C::B_DQFULL));
+        tc_commit_warp(bar(C::B_STEMPTY + s));
+        tc_commit_warp(bar(C::B_MMADONE));
       }
-      tc_commit(bar(C::B_DRAIN));
-      mbar_wait_drain(bar(C::B_DRAIN), 0, wc);
+      tc_commit_warp(bar(C::B_DRAIN));
+      mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
     }
   } else if (warp < 6) {
     // ------------------------------------------------------------ P / dS math

@@ -19,7 +19,8 @@
 // Mapping to the hardware (one CTA = two 128-row query tiles, 12 warps):
 //   warp 0      TMA producer: both Q tiles once, then K_j, V_j through a
 //               STAGES-deep ring of shared-memory slots (full/empty mbarriers).
-//   warp 1      TMEM allocator and single-thread tcgen05.mma issuer:
+//   warp 1      TMEM allocator and tcgen05.mma issuer (the converged warp runs
+//               the loop, one elected lane issues):
 //               S_t = Q_t K_j^T  (SS MMA, M=128 N=128, TMEM buffer t)
 //               O_t += P_t V_j   (TS MMA, P_t read from TMEM, V from smem)
 //   warps 4..7  softmax of query tile 0, warps 8..11 of tile 1: thread r owns
@@ -161,13 +162,14 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    } else if (warp == 1 && lane == 0) {
+    } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
-      bool ok = mbar_wait(bar(C::B_QFULL), 0, wc);
+      // The whole warp runs this loop (uniform operands); one elected lane issues.
+      bool ok = mbar_wait_warp(bar(C::B_QFULL), 0, wc);
       tc_fence_after();
       auto kv_slot = [&](int li) -> int { return li % C::STAGES; };
       auto wait_kv = [&](int li) -> bool {
-        if (!mbar_wait(bar(C::B_KVFULL + kv_slot(li)), (li / C::STAGES) & 1, wc)) return false;
+        if (!mbar_wait_warp(bar(C::B_KVFULL + kv_slot(li)), (li / C::STAGES) & 1, wc)) return false;
         tc_fence_after();
         return true;
       };
@@ -178,57 +180,57 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          mma_ss(tmem + C::TM_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
-                 sdesc_sw128(kb + off, 16, 1024), C::IDESC_S, kk > 0);
+          mma_ss_warp(tmem + C::TM_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
+                      sdesc_sw128(kb + off, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
         }
-        tc_commit(bar(C::B_SFULL + t));
+        tc_commit_warp(bar(C::B_SFULL + t));
       };
       // O_t += P_t V (A = 16 keys of P = 8 TMEM columns; B = 16 V rows, MN-major).
       auto issue_pv = [&](int t, int li, bool acc) {
         const uint32_t vb = sKV + kv_slot(li) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts(tmem + C::TM_O + t * D, tmem + C::TM_S + t * 128 + kk * 8,
-                 sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
-                 (acc || kk > 0) ? 1u : 0u);
-        tc_commit(bar(C::B_ODONE + t));
+          mma_ts_warp(tmem + C::TM_O + t * D, tmem + C::TM_S + t * 128 + kk * 8,
+                      sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
+                      (kk > 0 || acc) ? 1u : 0u);
+        tc_commit_warp(bar(C::B_ODONE + t));
       };
       if (ok && (ok = wait_kv(0))) {
         issue_s(0, 0);
         issue_s(1, 0);
-        tc_commit(bar(C::B_KVEMPTY + kv_slot(0)));
+        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(0)));
       }
       for (int j = 0; j < n_kv && ok; ++j) {
         const int liK = 2 * (j + 1), liV = 2 * j + 1;
         const bool more = j + 1 < n_kv;
         if (!wait_kv(liV)) break;
         for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait(bar(C::B_PFULL + t), j & 1, wc)) {
+          if (!mbar_wait_warp(bar(C::B_PFULL + t), j & 1, wc)) {
             ok = false;
             break;
           }
           tc_fence_after();
           issue_pv(t, liV, j > 0);
-          if (t == 1) tc_commit(bar(C::B_KVEMPTY + kv_slot(liV)));
+          if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liV)));
           if (more) {
             if (t == 0 && !wait_kv(liK)) {
               ok = false;
               break;
             }
             // S buffer t holds P_t of this tile until P_t V has completed.
-            if (!mbar_wait(bar(C::B_ODONE + t), j & 1, wc)) {
+            if (!mbar_wait_warp(bar(C::B_ODONE + t), j & 1, wc)) {
               ok = false;
               break;
             }
             tc_fence_after();
             issue_s(t, liK);
-            if (t == 1) tc_commit(bar(C::B_KVEMPTY + kv_slot(liK)));
+            if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liK)));
           }
         }
       }
-      // Drain: all MMAs of this thread complete before TMEM is released.
-      tc_commit(bar(C::B_DRAIN));
-      mbar_wait_drain(bar(C::B_DRAIN), 0, wc);
+      // Drain: all MMAs of this warp complete before TMEM is released.
+      tc_commit_warp(bar(C::B_DRAIN));
+      mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
     }
   } else {
     regs_inc<kRegsHigh>();

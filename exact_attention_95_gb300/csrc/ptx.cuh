@@ -296,3 +296,50 @@ __device__ __forceinline__ void grouped_order(int linear, int heads, int tiles, 
 }
 
 }  // namespace attn
+
+namespace attn {
+
+// Warp-wide variants for a convergent issuing warp: every lane executes the
+// call with the same operands and one elected lane issues the instruction.
+// Issuing from a converged warp keeps the operands in uniform registers, which
+// roughly halves the cost of each tcgen05.mma issue compared with a single
+// divergent lane.
+__device__ __forceinline__ void mma_ss_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void tc_commit_warp(uint32_t bar) {
+  asm volatile(
+      "{\n\t.reg .pred e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "@e tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}\n" ::"r"(
+          bar)
+      : "memory");
+}
+// Bounded wait by a whole warp with a warp-uniform result.
+__device__ __forceinline__ bool mbar_wait_warp(uint32_t bar, uint32_t parity, const WaitCtx& ctx) {
+  const bool ok = mbar_wait(bar, parity, ctx);
+  return __all_sync(0xffffffffu, ok);
+}
+__device__ __forceinline__ bool mbar_wait_drain_warp(uint32_t bar, uint32_t parity, const WaitCtx& ctx) {
+  const bool ok = mbar_wait_drain(bar, parity, ctx);
+  return __all_sync(0xffffffffu, ok);
+}
+
+}  // namespace attn
