@@ -202,10 +202,11 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
   int* status = status_ptr();
   if (!status) return ATTN_ERR_CUDA;
   CUtensorMap tq, tk, tv, tdo;
-  if (!make_map(&tq, Q, (long long)B * Hq, N, d, 64) || !make_map(&tdo, dO, (long long)B * Hq, N, d, 64) ||
+  // Query-side tiles of the backward are 128 rows, like the key-side tiles.
+  if (!make_map(&tq, Q, (long long)B * Hq, N, d, 128) || !make_map(&tdo, dO, (long long)B * Hq, N, d, 128) ||
       !make_map(&tk, K, (long long)B * Hkv, N, d, 128) || !make_map(&tv, V, (long long)B * Hkv, N, d, 128))
     return ATTN_ERR_CUDA;
-  const int Npad = (N + 63) / 64 * 64;
+  const int Npad = (N + bwd_row_padding() - 1) / bwd_row_padding() * bwd_row_padding();
   BwdParams p{};
   p.Q = static_cast<const uint16_t*>(Q);
   p.K = static_cast<const uint16_t*>(K);

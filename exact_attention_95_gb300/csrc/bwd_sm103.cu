@@ -15,20 +15,28 @@
 //   bwd_pre     D_i = rowsum(dO * O) and LSE_i * log2(e) into the workspace;
 //               zeroes the fp32 dQ accumulator.
 //   bwd_main    one CTA per (batch, kv head, 128-key tile); loops over the G
-//               query heads of the group and the 64-row query tiles.  All
-//               five products run on tcgen05 with TMEM accumulators:
-//                 S^T  = K Q^T         (M=128 keys, N=64 queries)
-//                 dP^T = V dO^T
-//                 dV  += P^T dO        (P^T from TMEM, bf16)
-//                 dK  += dS^T Q        (dS^T from TMEM, bf16)
-//                 dQ^T = K^T dS^T      (dS^T from shared memory; M = d)
+//               query heads of the group and their 128-row query tiles.  Five
+//               tcgen05 products per query tile, all M=128 N=128:
+//                 S^T  = K Q^T         -> TMEM region S   (keys on lanes)
+//                 dP^T = V dO^T        -> TMEM region DP
+//                 dV  += P^T dO        (P^T read from region S as bf16)
+//                 dK  += dS^T Q        (dS^T read from region S as bf16)
+//                 dQ^T = K^T dS^T      (dS^T from shared memory) -> region DP
 //               dK and dV stay in TMEM across the whole group (no atomics);
-//               dQ^T is read back by a second warpgroup and reduce-added
-//               (fp32) into the accumulator.
+//               dQ^T is read back and reduce-added (fp32) into the accumulator.
 //   bwd_dq      dQ = bf16(scale * accumulator).
-// Warps of bwd_main: 0 TMA producer, 1 TMEM allocator + MMA issuer,
-// 2..5 probability/gradient math (thread = key row), 6..9 dQ readback
-// (thread = head-dim index).
+//
+// Warps of bwd_main (12): 0 TMA producer, 1 TMEM allocator + MMA issuer
+// (converged warp, elected lane issues), 2-3 idle, 4-7 and 8-11 two math
+// warpgroups: thread = key row (TMEM lane), warpgroup h owns query columns
+// [64h, 64h + 64) of every tile.  A math thread turns its 64 scores into P
+// (bf16, written over the first half of its own score columns), then its 64
+// dP values into dS (bf16, over the second half, and into shared memory for
+// the dQ product), then reads 64 columns of dQ^T (lane = head-dim index) and
+// adds them to the accumulator.
+// Shared memory: K and V tiles, two stages of (Q tile, dO tile, LSE, D).  dS
+// for the dQ product is written over the stage's dO tile once dV (the last
+// reader of dO) has completed.
 #include <algorithm>
 
 #include "kernels.h"
@@ -38,37 +46,42 @@ namespace attn {
 namespace {
 
 constexpr int kBK = 128;  // keys per CTA
-constexpr int kBQ = 64;   // query rows per inner tile
-constexpr int kMainThreads = 320;
+constexpr int kBQ = 128;  // query rows per inner tile
+constexpr int kMainThreads = 384;
+constexpr int kLaunchRegs = 168;  // per-thread registers of a 384-thread CTA
+constexpr int kRegsLow = 72;
+constexpr int kRegsHigh = 216;
+static_assert(128 * kRegsLow + 256 * kRegsHigh <= kMainThreads * kLaunchRegs,
+              "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 
 template <int D>
 struct Bwd {
   static constexpr int CB = D / 64;
-  static constexpr int KBLK = kBK * 128;  // 128 rows x 128 bytes
-  static constexpr int QBLK = kBQ * 128;  // 64 rows x 128 bytes
+  static constexpr int BLK = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int OFF_K = 0;
-  static constexpr int OFF_V = OFF_K + CB * KBLK;
-  static constexpr int OFF_DS = OFF_V + CB * KBLK;  // dS^T, 128 keys x 64 queries bf16
-  static constexpr int OFF_STAGE = OFF_DS + kBK * 128;
+  static constexpr int OFF_V = OFF_K + CB * BLK;
+  static constexpr int OFF_STAGE = OFF_V + CB * BLK;
   static constexpr int ST_Q = 0;
-  static constexpr int ST_DO = CB * QBLK;
-  static constexpr int ST_LSE = 2 * CB * QBLK;
+  static constexpr int ST_DO = CB * BLK;  // >= 2 blocks: also holds dS^T (128 keys x 128 queries)
+  static constexpr int DO_BYTES = (CB < 2 ? 2 : CB) * BLK;
+  static constexpr int ST_LSE = ST_DO + DO_BYTES;
   static constexpr int ST_D = ST_LSE + kBQ * 4;
   static constexpr int STAGE_BYTES = (ST_D + kBQ * 4 + 1023) / 1024 * 1024;
   static constexpr int STAGES = 2;
   static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int B_KVFULL = 0;
-  static constexpr int B_STFULL = 1;               // STAGES
+  static constexpr int B_STFULL = 1;  // STAGES
   static constexpr int B_STEMPTY = B_STFULL + STAGES;
   static constexpr int B_SFULL = B_STEMPTY + STAGES;
   static constexpr int B_DPFULL = B_SFULL + 1;
   static constexpr int B_PFULL = B_DPFULL + 1;
-  static constexpr int B_DSFULL = B_PFULL + 1;
-  static constexpr int B_DQFULL = B_DSFULL + 1;
+  static constexpr int B_DVDONE = B_PFULL + 1;
+  static constexpr int B_DSFULL = B_DVDONE + 1;
+  static constexpr int B_KVDONE = B_DSFULL + 1;
+  static constexpr int B_DQFULL = B_KVDONE + 1;
   static constexpr int B_DQFREE = B_DQFULL + 1;
-  static constexpr int B_MMADONE = B_DQFREE + 1;
-  static constexpr int B_DRAIN = B_MMADONE + 1;
+  static constexpr int B_DRAIN = B_DQFREE + 1;
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
@@ -76,9 +89,8 @@ struct Bwd {
   // TMEM columns
   static constexpr uint32_t TM_DV = 0;
   static constexpr uint32_t TM_DK = D;
-  static constexpr uint32_t TM_S = 2 * D;
-  static constexpr uint32_t TM_DP = 2 * D + 64;
-  static constexpr uint32_t TM_DQ = 2 * D + 128;
+  static constexpr uint32_t TM_S = 2 * D;         // 128 columns: S^T, then P | dS (bf16)
+  static constexpr uint32_t TM_DP = 2 * D + 128;  // 128 columns: dP^T, then dQ^T
   static constexpr uint32_t IDESC_ST = idesc_bf16(128, kBQ, false, false);
   static constexpr uint32_t IDESC_KV = idesc_bf16(128, D, false, true);
   static constexpr uint32_t IDESC_DQ = idesc_bf16(128, kBQ, true, true);
@@ -159,7 +171,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   auto bar = [&](int i) -> uint32_t { return sb + C::OFF_BAR + 8 * i; };
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_TMEMSLOT);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_ABORT);
-  const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sDS = sb + C::OFF_DS;
+  const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V;
+  auto stage = [&](int s) -> uint32_t { return sb + C::OFF_STAGE + s * C::STAGE_BYTES; };
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -173,9 +186,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int hk = bhk - b * p.Hkv;
   const int G = p.Hq / p.Hkv;
   const int n_q = (p.N + kBQ - 1) / kBQ;
-  const int i0 = p.causal ? min(n_q, (k0 / kBQ)) : 0;  // first query tile that sees these keys
+  const int i0 = p.causal ? (k0 / kBQ) : 0;  // first query tile that sees these keys
   const int per_head = n_q - i0;
-  const int T = G * per_head;  // inner iterations
+  const int T = G * per_head;  // inner iterations (>= 1 since k0 < N)
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KVFULL), 1);
@@ -185,11 +198,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
-    mbar_init(bar(C::B_PFULL), 128);
-    mbar_init(bar(C::B_DSFULL), 128);
+    mbar_init(bar(C::B_PFULL), 256);
+    mbar_init(bar(C::B_DVDONE), 1);
+    mbar_init(bar(C::B_DSFULL), 256);
+    mbar_init(bar(C::B_KVDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
-    mbar_init(bar(C::B_DQFREE), 128);
-    mbar_init(bar(C::B_MMADONE), 1);
+    mbar_init(bar(C::B_DQFREE), 256);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -204,17 +218,18 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.wait_limit_ns};
 
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
+  if (warp < 4) {
+    regs_dec<kRegsLow>();
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
-      mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::CB * C::KBLK);
+      mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::CB * C::BLK);
       for (int cb = 0; cb < C::CB; ++cb) {
-        tma_load_3d(sK + cb * C::KBLK, &tmK, bar(C::B_KVFULL), cb * 64, k0, bhk);
-        tma_load_3d(sV + cb * C::KBLK, &tmV, bar(C::B_KVFULL), cb * 64, k0, bhk);
+        tma_load_3d(sK + cb * C::BLK, &tmK, bar(C::B_KVFULL), cb * 64, k0, bhk);
+        tma_load_3d(sV + cb * C::BLK, &tmV, bar(C::B_KVFULL), cb * 64, k0, bhk);
       }
       int t = 0;
       for (; t < T; ++t) {
@@ -223,12 +238,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int g = t / per_head;
         const int it = i0 + (t - g * per_head);
         const int bhq = b * p.Hq + hk * G + g;
-        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+        const uint32_t st = stage(s);
         const uint32_t fb = bar(C::B_STFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * C::CB * C::QBLK + 2 * kBQ * 4);
+        mbar_arrive_expect_tx(fb, 2 * C::CB * C::BLK + 2 * kBQ * 4);
         for (int cb = 0; cb < C::CB; ++cb) {
-          tma_load_3d(st + C::ST_Q + cb * C::QBLK, &tmQ, fb, cb * 64, it * kBQ, bhq);
-          tma_load_3d(st + C::ST_DO + cb * C::QBLK, &tmdO, fb, cb * 64, it * kBQ, bhq);
+          tma_load_3d(st + C::ST_Q + cb * C::BLK, &tmQ, fb, cb * 64, it * kBQ, bhq);
+          tma_load_3d(st + C::ST_DO + cb * C::BLK, &tmdO, fb, cb * 64, it * kBQ, bhq);
         }
         const size_t vo = (size_t)bhq * p.Npad + (size_t)it * kBQ;
         asm volatile(
@@ -245,131 +260,138 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       mbar_wait_drain(bar(C::B_KVFULL), 0, wc);
       for (int k = max(0, t - C::STAGES); k < t; ++k)
         mbar_wait_drain(bar(C::B_STFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    {
+    } else if (warp == 1) {
+      // ---------------------------------------------------------- MMA issuer
       // The whole warp runs this loop (uniform operands); one elected lane issues.
       bool ok = mbar_wait_warp(bar(C::B_KVFULL), 0, wc);
       for (int t = 0; t < T && ok; ++t) {
         const int s = t % C::STAGES;
-        const uint32_t st = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+        const uint32_t st = stage(s);
+        const uint32_t qs = st + C::ST_Q, dos = st + C::ST_DO;
         if (!mbar_wait_warp(bar(C::B_STFULL + s), (t / C::STAGES) & 1, wc)) break;
-        // All MMAs of the previous iteration are complete: the S/P, dP/dS
-        // TMEM regions and the dS shared-memory tile may be overwritten.
-        if (t > 0 && !mbar_wait_warp(bar(C::B_MMADONE), (t - 1) & 1, wc)) break;
+        // Region S is free once dV and dK of the previous tile have completed.
+        if (t > 0 && !mbar_wait_warp(bar(C::B_KVDONE), (t - 1) & 1, wc)) break;
         tc_fence_after();
-        // S^T = K Q^T and dP^T = V dO^T (both K-major operands).
+        // S^T = K Q^T (both K-major; 16 head-dim columns per step).
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::KBLK + (kk & 3) * 32;
-          const uint32_t qa = (kk >> 2) * C::QBLK + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::TM_S, sdesc_sw128(sK + ka, 16, 1024), sdesc_sw128(st + C::ST_Q + qa, 16, 1024),
-                 C::IDESC_ST, kk > 0);
+          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+          mma_ss_warp(tmem + C::TM_S, sdesc_sw128(sK + off, 16, 1024), sdesc_sw128(qs + off, 16, 1024),
+                      C::IDESC_ST, kk > 0 ? 1u : 0u);
         }
         tc_commit_warp(bar(C::B_SFULL));
+        // Region DP is free once the previous dQ^T has been read back.
+        if (t > 0 && !mbar_wait_warp(bar(C::B_DQFREE), (t - 1) & 1, wc)) break;
+        tc_fence_after();
+        // dP^T = V dO^T.
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t ka = (kk >> 2) * C::KBLK + (kk & 3) * 32;
-          const uint32_t qa = (kk >> 2) * C::QBLK + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::TM_DP, sdesc_sw128(sV + ka, 16, 1024),
-                 sdesc_sw128(st + C::ST_DO + qa, 16, 1024), C::IDESC_ST, kk > 0);
+          const uint32_t off = (kk >> 2) * C::BLK + (kk & 3) * 32;
+          mma_ss_warp(tmem + C::TM_DP, sdesc_sw128(sV + off, 16, 1024), sdesc_sw128(dos + off, 16, 1024),
+                      C::IDESC_ST, kk > 0 ? 1u : 0u);
         }
         tc_commit_warp(bar(C::B_DPFULL));
-        // dV += P^T dO  (A = P^T in TMEM, B = dO MN-major: 16 query rows = 2048 bytes)
+        // dV += P^T dO: 16 queries per step; P of query columns [64h, 64h+64)
+        // sits in region S columns [64h, 64h+32) as packed bf16 pairs.
         if (!mbar_wait_warp(bar(C::B_PFULL), t & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts_warp(tmem + C::TM_DV, tmem + C::TM_S + kk * 8,
-                 sdesc_sw128(st + C::ST_DO + kk * 2048, C::QBLK, 1024), C::IDESC_KV,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        // dK += dS^T Q
+          mma_ts_warp(tmem + C::TM_DV, tmem + C::TM_S + (kk >> 2) * 64 + (kk & 3) * 8,
+                      sdesc_sw128(dos + kk * 2048, C::BLK, 1024), C::IDESC_KV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_warp(bar(C::B_DVDONE));
+        // dK += dS^T Q (dS in region S columns [64h+32, 64h+64)).
         if (!mbar_wait_warp(bar(C::B_DSFULL), t & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
-          mma_ts_warp(tmem + C::TM_DK, tmem + C::TM_DP + kk * 8,
-                 sdesc_sw128(st + C::ST_Q + kk * 2048, C::QBLK, 1024), C::IDESC_KV,
-                 (t > 0 || kk > 0) ? 1u : 0u);
-        // dQ^T = K^T dS^T  (A = K as MN-major [d x keys], B = dS^T MN-major [keys x queries]).
-        // For d = 64 the instruction still has M = 128; lanes 64..127 read the
-        // V tile as filler and are ignored.
-        if (t > 0 && !mbar_wait_warp(bar(C::B_DQFREE), (t - 1) & 1, wc)) break;
-        tc_fence_after();
+          mma_ts_warp(tmem + C::TM_DK, tmem + C::TM_S + (kk >> 2) * 64 + 32 + (kk & 3) * 8,
+                      sdesc_sw128(qs + kk * 2048, C::BLK, 1024), C::IDESC_KV,
+                      (t > 0 || kk > 0) ? 1u : 0u);
+        tc_commit_warp(bar(C::B_KVDONE));
+        // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS^T in the dO
+        // slot, MN-major [keys x queries] (two 64-query blocks).  For d = 64
+        // the product still has M = 128; lanes 64..127 read the V tile as
+        // filler and are discarded.
 #pragma unroll
         for (int kk = 0; kk < kBK / 16; ++kk)
-          mma_ss_warp(tmem + C::TM_DQ, sdesc_sw128(sK + kk * 2048, C::KBLK, 1024),
-                 sdesc_sw128(sDS + kk * 2048, 8192, 1024), C::IDESC_DQ, kk > 0);
+          mma_ss_warp(tmem + C::TM_DP, sdesc_sw128(sK + kk * 2048, C::BLK, 1024),
+                      sdesc_sw128(dos + kk * 2048, C::BLK, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
         tc_commit_warp(bar(C::B_DQFULL));
         tc_commit_warp(bar(C::B_STEMPTY + s));
-        tc_commit_warp(bar(C::B_MMADONE));
       }
       tc_commit_warp(bar(C::B_DRAIN));
       mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
     }
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ P / dS math
+  } else {
+    regs_inc<kRegsHigh>();
+    // ------------------------------------------------------------ math warpgroups
+    const int h = (warp - 4) >> 2;  // query-column half of this warpgroup
     const int quad = warp & 3;
-    const int kr = quad * 32 + lane;  // key row within the tile
+    const int kr = quad * 32 + lane;  // key row (TMEM lane) of the S / dP regions
     const int key = k0 + kr;
     const bool key_ok = key < p.N;
+    const int dcol = kr;  // head-dim index (TMEM lane) of the dQ^T region
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
+    const uint32_t tS = tmem + lane_off + C::TM_S + 64 * h;
+    const uint32_t tDP = tmem + lane_off + C::TM_DP + 64 * h;
     const float sl2 = p.scale_log2;
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
       const int g = t / per_head;
       const int it = i0 + (t - g * per_head);
-      const int q0 = it * kBQ;
-      const uint32_t stp = sb + C::OFF_STAGE + s * C::STAGE_BYTES;
+      const int qh0 = it * kBQ + 64 * h;  // first query column of this half
+      const int bhq = b * p.Hq + hk * G + g;
+      const uint32_t st = stage(s);
       if (!mbar_wait(bar(C::B_STFULL + s), (t / C::STAGES) & 1, wc) ||
           !mbar_wait(bar(C::B_SFULL), t & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
+      // ---- P = 2^(s * scale * log2e - LSE2) for 64 query columns.
       uint32_t sr[2][32];
-      tmem_ld32(tmem + lane_off + C::TM_S, sr[0]);
-      tmem_ld32(tmem + lane_off + C::TM_S + 32, sr[1]);
+      tmem_ld32(tS, sr[0]);
+      tmem_ld32(tS + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       reg_fence32(sr[1]);
-      const bool diag = p.causal && (q0 < k0 + kBK - 1);
+      const bool diag = p.causal && (qh0 < k0 + kBK - 1);
       float pv[64];
       uint32_t pk[32];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 lq = lds_f4(stp + C::ST_LSE + 16 * c4);  // same address in every lane
+        const float4 lq = lds_f4(st + C::ST_LSE + 4 * (64 * h + 4 * c4));  // same address in all lanes
         const float l4[4] = {lq.x, lq.y, lq.z, lq.w};
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           const int c = 4 * c4 + u;
           float x = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -l4[u]));
-          if (!key_ok || (diag && key > q0 + c)) x = 0.f;
+          if (!key_ok || (diag && key > qh0 + c)) x = 0.f;
           pv[c] = x;
         }
       }
 #pragma unroll
       for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
-      tmem_st32(tmem + lane_off + C::TM_S, pk);
+      tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_PFULL));
-
+      // ---- dS = P (dP - D), 32 columns at a time.
       if (!mbar_wait(bar(C::B_DPFULL), t & 1, wc)) {
         ok = false;
         break;
       }
       tc_fence_after();
-      // dS = P (dP - D), one half of the 64 query columns at a time.
 #pragma unroll
       for (int half = 0; half < 2; ++half) {
         uint32_t dr[32];
-        tmem_ld32(tmem + lane_off + C::TM_DP + 32 * half, dr);
+        tmem_ld32(tDP + 32 * half, dr);
         tmem_ld_wait(dr);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dq = lds_f4(stp + C::ST_D + 128 * half + 16 * c4);
+          const float4 dq = lds_f4(st + C::ST_D + 4 * (64 * h + 32 * half + 4 * c4));
           const int c = 32 * half + 4 * c4;
           pk[16 * half + 2 * c4] = pack_bf16(pv[c] * (__uint_as_float(dr[4 * c4]) - dq.x),
                                              pv[c + 1] * (__uint_as_float(dr[4 * c4 + 1]) - dq.y));
@@ -377,14 +399,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                                                  pv[c + 3] * (__uint_as_float(dr[4 * c4 + 3]) - dq.w));
         }
       }
-      tmem_st32(tmem + lane_off + C::TM_DP, pk);
-      // dS^T row into shared memory for the dQ product (128-byte swizzle: the
-      // 16-byte chunk c of row kr lives at chunk position c ^ (kr & 7)).
-      if (t > 0 && !mbar_wait(bar(C::B_DQFULL), (t - 1) & 1, wc)) {
+      tmem_st32(tS + 32, pk);
+      // dS^T rows into the dO slot (dV, its last reader, must be complete):
+      // block h holds query columns [64h, 64h+64); row kr is 128 bytes with
+      // the 16-byte chunk c stored at chunk position c ^ (kr & 7).
+      if (!mbar_wait(bar(C::B_DVDONE), t & 1, wc)) {
         ok = false;
         break;
       }
-      const uint32_t dsrow = sDS + kr * 128;
+      const uint32_t dsrow = st + C::ST_DO + h * C::BLK + kr * 128;
 #pragma unroll
       for (int c = 0; c < 8; ++c)
         sts_u4(dsrow + ((c ^ (kr & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
@@ -392,23 +415,43 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_DSFULL));
+      // ---- dQ^T readback: 64 query columns of head-dim row dcol.
+      if (!mbar_wait(bar(C::B_DQFULL), t & 1, wc)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t qr[2][32];
+      tmem_ld32(tDP, qr[0]);
+      tmem_ld32(tDP + 32, qr[1]);
+      tmem_ld_wait(qr[0]);
+      reg_fence32(qr[1]);
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DQFREE));
+      if (dcol < D) {
+        float* acc = p.dQacc + ((size_t)bhq * p.Npad + (size_t)qh0) * D + dcol;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) atomicAdd(acc + (size_t)c * D, __uint_as_float(qr[c >> 5][c & 31]));
+      }
     }
-    // Epilogue: dV and scale * dK rows of this key tile.
-    if (ok && T > 0 && mbar_wait(bar(C::B_MMADONE), (T - 1) & 1, wc)) {
+    // Epilogue: dV and scale * dK rows of this key tile; warpgroup h writes
+    // head-dim columns [h*D/2, (h+1)*D/2).
+    if (ok && mbar_wait(bar(C::B_KVDONE), (T - 1) & 1, wc)) {
       tc_fence_after();
       const size_t row = (size_t)bhk * p.N + key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
         uint16_t* dst = (which == 0 ? p.dV : p.dK) + row * D;
         const float mul = which == 0 ? 1.f : p.scale;
-        const uint32_t base = which == 0 ? C::TM_DV : C::TM_DK;
+        const uint32_t base = tmem + lane_off + (which == 0 ? C::TM_DV : C::TM_DK);
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
+        for (int c = 0; c < D / 64; ++c) {
+          const int col = h * (D / 2) + 32 * c;
           uint32_t o[32];
-          tmem_ld32(tmem + lane_off + base + c * 32, o);
+          tmem_ld32(base + col, o);
           tmem_ld_wait(o);
           if (key_ok) {
-            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 32);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint4 v;
@@ -420,34 +463,6 @@ __global__ void __launch_bounds__(kMainThreads, 1)
             }
           }
         }
-      }
-    } else if (T == 0 && key_ok) {
-      // No query tile reaches these keys (cannot happen when Nq = Nk): zero grads.
-      const size_t row = (size_t)bhk * p.N + key;
-      for (int c = 0; c < D; ++c) p.dV[row * D + c] = p.dK[row * D + c] = 0;
-    }
-  } else {
-    // ------------------------------------------------------------ dQ readback
-    const int quad = warp & 3;
-    const int dcol = quad * 32 + lane;  // head-dim index (TMEM lane of dQ^T)
-    const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    for (int t = 0; t < T; ++t) {
-      const int g = t / per_head;
-      const int it = i0 + (t - g * per_head);
-      const int bhq = b * p.Hq + hk * G + g;
-      if (!mbar_wait(bar(C::B_DQFULL), t & 1, wc)) break;
-      tc_fence_after();
-      uint32_t r[2][32];
-      tmem_ld32(tmem + lane_off + C::TM_DQ, r[0]);
-      tmem_ld32(tmem + lane_off + C::TM_DQ + 32, r[1]);
-      tmem_ld_wait(r[0]);
-      reg_fence32(r[1]);
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DQFREE));
-      if (dcol < D) {
-        float* acc = p.dQacc + ((size_t)bhq * p.Npad + (size_t)it * kBQ) * D + dcol;
-#pragma unroll
-        for (int c = 0; c < kBQ; ++c) atomicAdd(acc + (size_t)c * D, __uint_as_float(r[c >> 5][c & 31]));
       }
     }
   }
@@ -477,6 +492,15 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
   }
   if (stages & kBwdMain) {
     auto kern = bwd_main_kernel<D>;
+    // setmaxnreg moves registers inside the launch allocation; refuse to launch
+    // if the compiler gave the kernel a different per-thread count than assumed.
+    static int regs = -1;
+    if (regs < 0) {
+      cudaFuncAttributes fa;
+      if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+      regs = fa.numRegs;
+    }
+    if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(p.B * p.Hkv * ((p.N + kBK - 1) / kBK));
@@ -494,8 +518,10 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
 
 }  // namespace
 
+int bwd_row_padding() { return kBQ; }
+
 size_t bwd_workspace_bytes(int B, int Hq, int N, int d) {
-  const size_t Npad = (size_t)(N + 63) / 64 * 64;
+  const size_t Npad = (size_t)(N + kBQ - 1) / kBQ * kBQ;
   const size_t rows = (size_t)B * Hq * Npad;
   return (rows * d * 4 + 255) / 256 * 256 + 2 * ((rows * 4 + 255) / 256 * 256);
 }

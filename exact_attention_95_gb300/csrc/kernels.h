@@ -43,7 +43,7 @@ struct BwdParams {
   uint16_t* dQ;         // [B, Hq, N, d]
   uint16_t* dK;         // [B, Hkv, N, d]
   uint16_t* dV;
-  float* dQacc;         // workspace [B, Hq, Npad, d] fp32
+  float* dQacc;         // workspace [B, Hq, Npad, d] fp32 (Npad: N rounded up to 128)
   float* Dvec;          // workspace [B, Hq, Npad]  rowsum(dO * O)
   float* LSE2;          // workspace [B, Hq, Npad]  LSE * log2(e)
   int* status;
@@ -55,6 +55,8 @@ struct BwdParams {
   unsigned long long wait_limit_ns;
 };
 
+// Query rows are padded to a multiple of this in the backward workspace.
+int bwd_row_padding();
 // Workspace layout of the backward (bytes), all fp32: dQacc then D then LSE2.
 size_t bwd_workspace_bytes(int B, int Hq, int N, int d);
 
