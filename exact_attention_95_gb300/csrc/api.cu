@@ -66,6 +66,20 @@ bool make_map(CUtensorMap* m, const void* base, long long BH, int N, int d, int 
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D fp32 map over the backward's dQ accumulator [rows][d]: box (d, 64), no
+// swizzle; the target of bulk reduce-adds of 64-row tiles.
+bool make_acc_map(CUtensorMap* m, const void* base, long long rows, int d) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  cuuint32_t box[2] = {(cuuint32_t)d, 64};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shape checks shared by forward and backward.  Returns ATTN_OK or an error.
@@ -237,7 +251,9 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
   p.head_group = head_group_for((size_t)(Hq / Hkv) * N * d * (2 + 2 + 4), (long long)B * Hkv);
   if ((long long)B * Hkv * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   p.wait_limit_ns = wait_limit();
-  cudaError_t e = launch_bwd_bf16(d, tq, tk, tv, tdo, p, stages, static_cast<cudaStream_t>(stream));
+  CUtensorMap tacc;
+  if (!make_acc_map(&tacc, p.dQacc, (long long)rows, d)) return ATTN_ERR_CUDA;
+  cudaError_t e = launch_bwd_bf16(d, tq, tk, tv, tdo, tacc, p, stages, static_cast<cudaStream_t>(stream));
   if (e == cudaErrorNotSupported) return ATTN_ERR_UNSUPPORTED;
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }

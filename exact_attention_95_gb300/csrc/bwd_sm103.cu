@@ -27,13 +27,14 @@
 //   bwd_dq      dQ = bf16(scale * accumulator).
 //
 // Warps of bwd_main (12): 0 TMA producer, 1 TMEM allocator + MMA issuer
-// (converged warp, elected lane issues), 2-3 idle, 4-7 and 8-11 two math
+// (converged warp, elected lane issues), 2 dQ reducer, 3 idle, 4-7 and 8-11 two math
 // warpgroups: thread = key row (TMEM lane), warpgroup h owns query columns
 // [64h, 64h + 64) of every tile.  A math thread turns its 64 scores into P
 // (bf16, written over the first half of its own score columns), then its 64
 // dP values into dS (bf16, over the second half, and into shared memory for
-// the dQ product), then reads 64 columns of dQ^T (lane = head-dim index) and
-// adds them to the accumulator.
+// the dQ product), then reads 64 columns of dQ^T (lane = head-dim index),
+// and stages them in shared memory; warp 2 adds each staged half to the
+// accumulator with one bulk tensor reduce and then releases the stage.
 // Shared memory: K and V tiles, two stages of (Q tile, dO tile, LSE, D).  dS
 // for the dQ product is written over the stage's dO tile once dV (the last
 // reader of dO) has completed.
@@ -81,7 +82,8 @@ struct Bwd {
   static constexpr int B_KVDONE = B_DSFULL + 1;
   static constexpr int B_DQFULL = B_KVDONE + 1;
   static constexpr int B_DQFREE = B_DQFULL + 1;
-  static constexpr int B_DRAIN = B_DQFREE + 1;
+  static constexpr int B_DQSTAGED = B_DQFREE + 1;  // 2: one per math warpgroup
+  static constexpr int B_DRAIN = B_DQSTAGED + 2;
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
@@ -162,7 +164,7 @@ template <int D>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = Bwd<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -194,7 +196,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(bar(C::B_KVFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_STFULL + s), 1);
-      mbar_init(bar(C::B_STEMPTY + s), 1);
+      mbar_init(bar(C::B_STEMPTY + s), 1);  // arrived by the dQ reducer
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
@@ -204,6 +206,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(bar(C::B_KVDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 256);
+    mbar_init(bar(C::B_DQSTAGED + 0), 128);
+    mbar_init(bar(C::B_DQSTAGED + 1), 128);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -319,10 +323,34 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           mma_ss_warp(tmem + C::TM_DP, sdesc_sw128(sK + kk * 2048, C::BLK, 1024),
                       sdesc_sw128(dos + kk * 2048, C::BLK, 1024), C::IDESC_DQ, kk > 0 ? 1u : 0u);
         tc_commit_warp(bar(C::B_DQFULL));
-        tc_commit_warp(bar(C::B_STEMPTY + s));
       }
       tc_commit_warp(bar(C::B_DRAIN));
       mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------- dQ reducer
+      // Adds each staged dQ half-tile to the accumulator with one bulk tensor
+      // reduce and releases the stage once the reduces have read it.
+      for (int t = 0; t < T; ++t) {
+        const int s = t % C::STAGES;
+        const int g = t / per_head;
+        const int it = i0 + (t - g * per_head);
+        const int bhq = b * p.Hq + hk * G + g;
+        const uint32_t st = stage(s);
+        bool ok = true;
+        for (int h = 0; h < 2 && ok; ++h) {
+          if (!mbar_wait(bar(C::B_DQSTAGED + h), t & 1, wc)) {
+            ok = false;
+            break;
+          }
+          tma_reduce_add_2d(&tmDQ, st + (h == 0 ? C::ST_Q : C::ST_DO), 0,
+                            (int)((size_t)bhq * p.Npad + (size_t)it * kBQ + 64 * h));
+        }
+        bulk_commit_group();
+        if (!ok) break;
+        bulk_wait_read0();
+        mbar_arrive(bar(C::B_STEMPTY + s));
+      }
+      bulk_wait0();
     }
   } else {
     regs_inc<kRegsHigh>();
@@ -428,11 +456,17 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       reg_fence32(qr[1]);
       tc_fence_before();
       mbar_arrive(bar(C::B_DQFREE));
+      // Stage this half of dQ (64 query rows x d, fp32, row-major) in shared
+      // memory -- warpgroup 0 over the Q slot, warpgroup 1 over the dO slot,
+      // both free once dQ^T has completed -- and add it to the accumulator
+      // with one bulk tensor reduce.
+      const uint32_t qstage = st + (h == 0 ? C::ST_Q : C::ST_DO);
       if (dcol < D) {
-        float* acc = p.dQacc + ((size_t)bhq * p.Npad + (size_t)qh0) * D + dcol;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) atomicAdd(acc + (size_t)c * D, __uint_as_float(qr[c >> 5][c & 31]));
+        for (int c = 0; c < 64; ++c) sts_f32(qstage + (c * D + dcol) * 4, __uint_as_float(qr[c >> 5][c & 31]));
       }
+      fence_async_smem();
+      mbar_arrive(bar(C::B_DQSTAGED + h));
     }
     // Epilogue: dV and scale * dK rows of this key tile; warpgroup h writes
     // head-dim columns [h*D/2, (h+1)*D/2).
@@ -477,8 +511,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 
 template <int D>
 cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                   const CUtensorMap& tmdO, const BwdParams& p, unsigned stages,
-                   cudaStream_t stream) {
+                   const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p,
+                   unsigned stages, cudaStream_t stream) {
   using C = Bwd<D>;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
@@ -504,7 +538,7 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     dim3 grid(p.B * p.Hkv * ((p.N + kBK - 1) / kBK));
-    kern<<<grid, kMainThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmdO, p);
+    kern<<<grid, kMainThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmdO, tmDQ, p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & kBwdConvert) {
@@ -527,10 +561,10 @@ size_t bwd_workspace_bytes(int B, int Hq, int N, int d) {
 }
 
 cudaError_t launch_bwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmdO, const BwdParams& p,
-                            unsigned stages, cudaStream_t stream) {
-  if (d == 128) return launch<128>(tmQ, tmK, tmV, tmdO, p, stages, stream);
-  if (d == 64) return launch<64>(tmQ, tmK, tmV, tmdO, p, stages, stream);
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmDQ,
+                            const BwdParams& p, unsigned stages, cudaStream_t stream) {
+  if (d == 128) return launch<128>(tmQ, tmK, tmV, tmdO, tmDQ, p, stages, stream);
+  if (d == 64) return launch<64>(tmQ, tmK, tmV, tmdO, tmDQ, p, stages, stream);
   return cudaErrorInvalidValue;
 }
 

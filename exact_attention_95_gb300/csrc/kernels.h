@@ -63,8 +63,10 @@ size_t bwd_workspace_bytes(int B, int Hq, int N, int d);
 // Stages of the backward, launched in this order.
 enum : unsigned { kBwdPre = 1u, kBwdMain = 2u, kBwdConvert = 4u, kBwdAll = 7u };
 
+// tmDQ is a 2-D fp32 map over the dQ accumulator [B*Hq*Npad][d] with a
+// (d, 64) box and no swizzle (bulk reduce-add target).
 cudaError_t launch_bwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
-                            const CUtensorMap& tmV, const CUtensorMap& tmdO,
+                            const CUtensorMap& tmV, const CUtensorMap& tmdO, const CUtensorMap& tmDQ,
                             const BwdParams& p, unsigned stages, cudaStream_t stream);
 
 }  // namespace attn
