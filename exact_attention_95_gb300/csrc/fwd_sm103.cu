@@ -186,14 +186,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit_warp(bar(C::B_SFULL + t));
       };
       // O_t += P_t V (A = 16 keys of P = 8 TMEM columns; B = 16 V rows, MN-major).
-      auto issue_pv = [&](int t, int li, bool acc) {
+      auto issue_pv = [&](int t, int li, bool acc, bool last) {
         const uint32_t vb = sKV + kv_slot(li) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
           mma_ts_warp(tmem + C::TM_O + t * D, tmem + C::TM_S + t * 128 + kk * 8,
                       sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
                       (kk > 0 || acc) ? 1u : 0u);
-        tc_commit_warp(bar(C::B_ODONE + t));
+        if (last) tc_commit_warp(bar(C::B_ODONE + t));  // O_t final: one completion only
       };
       if (ok && (ok = wait_kv(0))) {
         issue_s(0, 0);
@@ -210,19 +210,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           tc_fence_after();
-          issue_pv(t, liV, j > 0);
+          issue_pv(t, liV, j > 0, !more);
           if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liV)));
           if (more) {
             if (t == 0 && !wait_kv(liK)) {
               ok = false;
               break;
             }
-            // S buffer t holds P_t of this tile until P_t V has completed.
-            if (!mbar_wait_warp(bar(C::B_ODONE + t), j & 1, wc)) {
-              ok = false;
-              break;
-            }
-            tc_fence_after();
+            // S_t of the next tile overwrites the TMEM columns P_t V reads.
+            // tcgen05.mma operations of one CTA execute in issue order, so the
+            // reads of P_t V precede the writes of the next S_t without a wait.
             issue_s(t, liK);
             if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liK)));
           }
@@ -289,7 +286,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
       if (j > 0 && __any_sync(0xffffffffu, move)) {
-        // O_t holds tiles < j (their P V completed before S_t of tile j was issued).
+        // O_t holds tiles < j: their P V precede S_t of tile j in the MMA
+        // order, and S_t of tile j has completed.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -327,7 +325,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_arrive(bar(C::B_PFULL + t));
     }
     // Epilogue: O / l and LSE.
-    if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
+    if (ok && mbar_wait(bar(C::B_ODONE + t), 0, wc)) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q < p.N;
