@@ -273,7 +273,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int i = 0; i < 32; ++i) mp[i & 7] = fmaxf(mp[i & 7], __uint_as_float(sr[c][i]));
+        for (int i = 0; i < 16; ++i)
+          mp[i & 7] = fmax3(mp[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
       const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
                              fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
       // Move m only when the tile's max exceeds it by more than the threshold.
@@ -298,9 +299,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_st32(o_t + c * 32, o);
         }
       }
-      float rs[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) rs[i] = 0.f;
+      // Row sums in four packed (f32x2) accumulators; x = s * scale*log2e - m
+      // for two columns per packed FMA.
+      uint64_t rs2[4] = {0, 0, 0, 0};
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      const uint64_t negm2 = f2pack(-m_use, -m_use);
       // P as packed bf16 pairs, stored in two halves of 32 TMEM columns: the
       // first half lands on S columns [0, 32), already read into registers.
 #pragma unroll
@@ -311,15 +314,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int c = 2 * half + cc;
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
-            const float p0 = ex2(fmaf(__uint_as_float(sr[c][2 * i]), sl2, -m_use));
-            const float p1 = ex2(fmaf(__uint_as_float(sr[c][2 * i + 1]), sl2, -m_use));
-            rs[i & 7] += p0 + p1;
+            float x0, x1;
+            f2unpack(ffma2(f2pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2,
+                           negm2),
+                     x0, x1);
+            const float p0 = ex2(x0);
+            const float p1 = ex2(x1);
+            rs2[i & 3] = fadd2(rs2[i & 3], f2pack(p0, p1));
             w[cc * 16 + i] = pack_bf16(p0, p1);
           }
         }
         tmem_st32(s_t + half * 32, w);
       }
-      l += ((rs[0] + rs[1]) + (rs[2] + rs[3])) + ((rs[4] + rs[5]) + (rs[6] + rs[7]));
+      {
+        float a0, a1;
+        f2unpack(fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3])), a0, a1);
+        l += a0 + a1;
+      }
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_PFULL + t));
