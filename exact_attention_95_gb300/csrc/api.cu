@@ -236,8 +236,8 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
   const size_t acc_bytes = (rows * d * 4 + 255) / 256 * 256;
   const size_t vec_bytes = (rows * 4 + 255) / 256 * 256;
   p.dQacc = reinterpret_cast<float*>(ws);
-  p.Dvec = reinterpret_cast<float*>(ws + acc_bytes);
-  p.LSE2 = reinterpret_cast<float*>(ws + acc_bytes + vec_bytes);
+  p.negD = reinterpret_cast<float*>(ws + acc_bytes);
+  p.negLSE2 = reinterpret_cast<float*>(ws + acc_bytes + vec_bytes);
   p.status = status;
   p.B = B;
   p.Hq = Hq;

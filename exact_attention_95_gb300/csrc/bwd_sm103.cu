@@ -12,8 +12,9 @@
 // with D_i = <dO_i, O_i>.
 //
 // Kernels:
-//   bwd_pre     D_i = rowsum(dO * O) and LSE_i * log2(e) into the workspace;
-//               zeroes the fp32 dQ accumulator.
+//   bwd_pre     -D_i = -rowsum(dO * O) and -LSE_i * log2(e) into the workspace
+//               (stored negated: the main kernel adds them); zeroes the fp32
+//               dQ accumulator.
 //   bwd_main    one CTA per (batch, kv head, 128-key tile); loops over the G
 //               query heads of the group and their 128-row query tiles.  Five
 //               tcgen05 products per query tile, all M=128 N=128:
@@ -99,8 +100,8 @@ struct Bwd {
 };
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (b, h, row) of the padded row range: D, LSE2, and a zeroed
-// accumulator row.  Rows past N get D = 0 and LSE2 = +inf (probability 0).
+// One warp per (b, h, row) of the padded row range: -D, -LSE * log2(e), and a
+// zeroed accumulator row.  Rows past N get D = 0 and -LSE2 = -inf (probability 0).
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   constexpr int EPL = D / 32;  // elements per lane
@@ -132,8 +133,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
     if (lane == 0) {
-      p.Dvec[r] = dsum;
-      p.LSE2[r] = i < p.N ? p.LSE[bh * p.N + i] * 1.4426950408889634f : INFINITY;
+      p.negD[r] = -dsum;
+      p.negLSE2[r] = i < p.N ? -p.LSE[bh * p.N + i] * 1.4426950408889634f : -INFINITY;
     }
     float4* acc = reinterpret_cast<float4*>(p.dQacc + r * D);
     for (int k = lane; k < D / 4; k += 32) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -253,12 +254,12 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 st + C::ST_LSE),
-            "l"(p.LSE2 + vo), "r"(kBQ * 4), "r"(fb)
+            "l"(p.negLSE2 + vo), "r"(kBQ * 4), "r"(fb)
             : "memory");
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 st + C::ST_D),
-            "l"(p.Dvec + vo), "r"(kBQ * 4), "r"(fb)
+            "l"(p.negD + vo), "r"(kBQ * 4), "r"(fb)
             : "memory");
       }
       mbar_wait_drain(bar(C::B_KVFULL), 0, wc);
@@ -379,34 +380,38 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         break;
       }
       tc_fence_after();
-      // ---- P = 2^(s * scale * log2e - LSE2) for 64 query columns.
+      // ---- P = 2^(s * scale * log2e - LSE2) for 64 query columns, two per
+      // packed FMA (the workspace holds -LSE2).
       uint32_t sr[2][32];
       tmem_ld32(tS, sr[0]);
       tmem_ld32(tS + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       reg_fence32(sr[1]);
       const bool diag = p.causal && (qh0 < k0 + kBK - 1);
-      float pv[64];
+      const uint64_t sl2x2 = f2pack(sl2, sl2);
+      uint64_t pv2[32];  // P, column pairs
       uint32_t pk[32];
 #pragma unroll
       for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 lq = lds_f4(st + C::ST_LSE + 4 * (64 * h + 4 * c4));  // same address in all lanes
-        const float l4[4] = {lq.x, lq.y, lq.z, lq.w};
+        const float4 nl = lds_f4(st + C::ST_LSE + 4 * (64 * h + 4 * c4));  // same address in all lanes
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int c = 4 * c4 + u;
-          float x = ex2(fmaf(__uint_as_float(sr[c >> 5][c & 31]), sl2, -l4[u]));
-          if (!key_ok || (diag && key > qh0 + c)) x = 0.f;
-          pv[c] = x;
+        for (int u = 0; u < 2; ++u) {
+          const int c = 4 * c4 + 2 * u;
+          const uint64_t s2 = f2pack(__uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]));
+          float x0, x1;
+          f2unpack(ffma2(s2, sl2x2, u == 0 ? f2pack(nl.x, nl.y) : f2pack(nl.z, nl.w)), x0, x1);
+          float p0 = ex2(x0), p1 = ex2(x1);
+          if (!key_ok || (diag && key > qh0 + c)) p0 = 0.f;
+          if (!key_ok || (diag && key > qh0 + c + 1)) p1 = 0.f;
+          pv2[c / 2] = f2pack(p0, p1);
+          pk[c / 2] = pack_bf16(p0, p1);
         }
       }
-#pragma unroll
-      for (int c = 0; c < 32; ++c) pk[c] = pack_bf16(pv[2 * c], pv[2 * c + 1]);
       tmem_st32(tS, pk);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_PFULL));
-      // ---- dS = P (dP - D), 32 columns at a time.
+      // ---- dS = P (dP - D), 32 columns at a time (the workspace holds -D).
       if (!mbar_wait(bar(C::B_DPFULL), t & 1, wc)) {
         ok = false;
         break;
@@ -419,12 +424,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tmem_ld_wait(dr);
 #pragma unroll
         for (int c4 = 0; c4 < 8; ++c4) {
-          const float4 dq = lds_f4(st + C::ST_D + 4 * (64 * h + 32 * half + 4 * c4));
-          const int c = 32 * half + 4 * c4;
-          pk[16 * half + 2 * c4] = pack_bf16(pv[c] * (__uint_as_float(dr[4 * c4]) - dq.x),
-                                             pv[c + 1] * (__uint_as_float(dr[4 * c4 + 1]) - dq.y));
-          pk[16 * half + 2 * c4 + 1] = pack_bf16(pv[c + 2] * (__uint_as_float(dr[4 * c4 + 2]) - dq.z),
-                                                 pv[c + 3] * (__uint_as_float(dr[4 * c4 + 3]) - dq.w));
+          const float4 nd = lds_f4(st + C::ST_D + 4 * (64 * h + 32 * half + 4 * c4));
+#pragma unroll
+          for (int u = 0; u < 2; ++u) {
+            const int cp = 16 * half + 2 * c4 + u;  // column pair index
+            const uint64_t dp2 = f2pack(__uint_as_float(dr[4 * c4 + 2 * u]), __uint_as_float(dr[4 * c4 + 2 * u + 1]));
+            const uint64_t ds2 = fmul2(pv2[cp], fadd2(dp2, u == 0 ? f2pack(nd.x, nd.y) : f2pack(nd.z, nd.w)));
+            float d0, d1;
+            f2unpack(ds2, d0, d1);
+            pk[cp] = pack_bf16(d0, d1);
+          }
         }
       }
       tmem_st32(tS + 32, pk);

@@ -44,8 +44,8 @@ struct BwdParams {
   uint16_t* dK;         // [B, Hkv, N, d]
   uint16_t* dV;
   float* dQacc;         // workspace [B, Hq, Npad, d] fp32 (Npad: N rounded up to 128)
-  float* Dvec;          // workspace [B, Hq, Npad]  rowsum(dO * O)
-  float* LSE2;          // workspace [B, Hq, Npad]  LSE * log2(e)
+  float* negD;          // workspace [B, Hq, Npad]  -rowsum(dO * O)
+  float* negLSE2;       // workspace [B, Hq, Npad]  -LSE * log2(e)
   int* status;
   int B, Hq, Hkv, N, Npad;
   float scale;          // softmax scale

@@ -405,3 +405,13 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
 }
 
 }  // namespace attn
+
+namespace attn {
+
+__device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+}  // namespace attn
