@@ -363,17 +363,29 @@ def run_native(args):
     return 0
 
 
+def kernel_source_sha(kernel_file):
+    """Hash of a kernel's source files, to tell whether a recorded capture is stale."""
+    import hashlib
+    csrc = os.path.join(ROOT, "exact_attention_95_gb300", "csrc")
+    h = hashlib.sha256()
+    for f in (kernel_file, "ptx.cuh", "kernels.h"):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
+
+
 def load_traffic(kernel_desc):
-    """DRAM bytes per launch of the dominant kernel from the committed ncu summary."""
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    summary, or None when there is none or the kernel changed since."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    key = "bwd_main" if kernel_desc.startswith("bwd_main") else "fwd"
+    key, src = ("bwd_main", "bwd_sm103.cu") if kernel_desc.startswith("bwd_main") else ("fwd", "fwd_sm103.cu")
     ent = d.get(key)
-    if not ent or ent.get("stale"):
+    if not ent or ent.get("source_sha256") != kernel_source_sha(src):
         return None
     return ent.get("bytes_per_launch")
 
