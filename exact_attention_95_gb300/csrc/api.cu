@@ -98,12 +98,13 @@ attn_status check_shape(int B, int Hq, int Hkv, int N, int d, float scale, int c
 unsigned long long wait_limit() { return kDefaultWaitLimitNs; }
 
 // Number of heads whose CTAs are scheduled together so that the operands they
-// share (about `bytes_per_head` each) stay resident in L2: a budget of 32 MiB.
-int head_group_for(size_t bytes_per_head, long long heads) {
-  const size_t budget = size_t(32) << 20;
-  long long g = bytes_per_head ? (long long)(budget / bytes_per_head) : 16;
+// share (about `bytes_per_head` each) stay resident in L2 (`budget` bytes of
+// the 126 MiB L2).  Fewer, larger groups shorten the tail: the heaviest CTAs of
+// the last group then start earlier.
+int head_group_for(size_t bytes_per_head, long long heads, size_t budget) {
+  long long g = bytes_per_head ? (long long)(budget / bytes_per_head) : 32;
   if (g < 1) g = 1;
-  if (g > 16) g = 16;
+  if (g > 32) g = 32;
   if (g > heads) g = heads;
   return (int)g;
 }
@@ -179,7 +180,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
   p.N = N;
   p.n_qtiles = (N + 127) / 128;
   p.n_pairs = (p.n_qtiles + 1) / 2;
-  p.head_group = head_group_for((size_t)N * d * 2 * 2, (long long)B * Hq);
+  p.head_group = head_group_for((size_t)N * d * 2 * 2, (long long)B * Hq, size_t(64) << 20);
   if ((long long)B * Hq * p.n_pairs > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   p.scale_log2 = sl2;
   p.causal = causal;
@@ -248,7 +249,8 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal;
   // Per kv head the CTAs share Q and dO (bf16) and the dQ accumulator (fp32) of its group.
-  p.head_group = head_group_for((size_t)(Hq / Hkv) * N * d * (2 + 2 + 4), (long long)B * Hkv);
+  p.head_group = head_group_for((size_t)(Hq / Hkv) * N * d * (2 + 2 + 4), (long long)B * Hkv,
+                                size_t(32) << 20);
   if ((long long)B * Hkv * ((N + 127) / 128) > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   p.wait_limit_ns = wait_limit();
   CUtensorMap tacc;

@@ -17,20 +17,23 @@
 // well as values <= 1.
 //
 // Mapping to the hardware (one CTA = two 128-row query tiles, 12 warps):
-//   warp 0      TMA producer: both Q tiles once, then K_j, V_j through a
-//               STAGES-deep ring of shared-memory slots (full/empty mbarriers).
+//   warp 0      TMA producer: both Q tiles once, then K and V tiles through a
+//               STAGES-deep ring of shared-memory slots (full/empty mbarriers),
+//               in use order: K_0, then K_{j+1} ahead of V_j.
 //   warp 1      TMEM allocator and tcgen05.mma issuer (the converged warp runs
 //               the loop, one elected lane issues):
-//               S_t = Q_t K_j^T  (SS MMA, M=128 N=128, TMEM buffer t)
-//               O_t += P_t V_j   (TS MMA, P_t read from TMEM, V from smem)
+//               S_t = Q_t K_j^T  (SS MMA, M=128 N=128) into ONE shared S buffer
+//               O_t += P_t V_j   (TS MMA, P_t from its own TMEM region)
 //   warps 4..7  softmax of query tile 0, warps 8..11 of tile 1: thread r owns
-//               row r; it reads S from TMEM (32x32b loads), keeps m and l in
-//               registers (log2 units), writes P as packed bf16 over the first
-//               64 columns of its S buffer, rescales its O row in TMEM when m
-//               moves, and finally writes O / l and LSE.
-// The two tiles ping-pong: while one warpgroup computes exponentials the
-// tensor pipe runs the other tile's P V and its next Q K^T.
-// TMEM columns: [0,128) S/P of tile 0, [128,256) of tile 1, then O_0, O_1.
+//               row r; it loads its S row from TMEM (32x32b loads) and at once
+//               releases the S buffer, so the other tile's next Q K^T runs
+//               while this tile computes its exponentials; it keeps m and l in
+//               registers (log2 units), writes P as packed bf16 into its own
+//               64-column region once its previous P V has completed, rescales
+//               its O row in TMEM when m moves, and finally writes O / l, LSE.
+// The S buffer alternates S_0(j), S_1(j), S_0(j+1), ...: while one warpgroup
+// computes exponentials the tensor pipe runs the other tile's P V and Q K^T.
+// TMEM columns: [0,128) S, [128,192) P_0, [192,256) P_1, then O_0, O_1.
 // Registers: warpgroup 0 gives registers to the two softmax warpgroups
 // (setmaxnreg), which hold a whole S row each.
 #include "kernels.h"
@@ -62,9 +65,10 @@ struct Fwd {
   static constexpr int B_QFULL = 0;
   static constexpr int B_KVFULL = 1;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
-  static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2
-  static constexpr int B_PFULL = B_SFULL + 2;         // 2
-  static constexpr int B_ODONE = B_PFULL + 2;         // 2
+  static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2: S buffer holds S_t
+  static constexpr int B_SFREE = B_SFULL + 2;         // S buffer read out (either tile)
+  static constexpr int B_PFULL = B_SFREE + 1;         // 2
+  static constexpr int B_ODONE = B_PFULL + 2;         // 2: P_t V complete
   static constexpr int B_DRAIN = B_ODONE + 2;
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
@@ -72,7 +76,8 @@ struct Fwd {
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + alignment slack
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t IDESC_O = idesc_bf16(kBM, D, false, true);
-  static constexpr uint32_t TM_S = 0;    // + 128 * t
+  static constexpr uint32_t TM_S = 0;    // one S buffer shared by both tiles (128 columns)
+  static constexpr uint32_t TM_P = 128;  // + 64 * t: P_t as packed bf16
   static constexpr uint32_t TM_O = 256;  // + D * t
 };
 
@@ -115,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(bar(C::B_PFULL + i), kBM);
       mbar_init(bar(C::B_ODONE + i), 1);
     }
+    mbar_init(bar(C::B_SFREE), kBM);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -141,22 +147,37 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(sQ + t * C::TILE_BYTES + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64,
                       q0 + t * kBM, bh);
+      // Load order follows use order: K_0, then K_{j+1} before V_j (the next
+      // Q K^T is issued before this tile's P V).
       int li = 0;
       bool ok = true;
-      for (int j = 0; j < n_kv && ok; ++j) {
-        for (int t = 0; t < 2; ++t, ++li) {
-          const int s = li % C::STAGES;
-          const uint32_t ph = (li / C::STAGES) & 1;
-          if (li >= C::STAGES && !mbar_wait(bar(C::B_KVEMPTY + s), ph ^ 1, wc)) {
-            ok = false;
-            break;
-          }
-          mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE_BYTES);
-          const CUtensorMap* m = t ? &tmV : &tmK;
-          for (int cb = 0; cb < C::CB; ++cb)
-            tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s),
-                        cb * 64, j * kBN, bh_kv);
+      for (int u = 0; u < 2 * n_kv && ok; ++u, ++li) {
+        int j;  // tile index of this load
+        bool v;
+        if (n_kv == 1) {
+          v = (u == 1);
+          j = 0;
+        } else if (u == 0) {
+          v = false;
+          j = 0;
+        } else if (u == 2 * n_kv - 1) {
+          v = true;
+          j = n_kv - 1;
+        } else {
+          v = (u % 2 == 0);
+          j = v ? u / 2 - 1 : (u + 1) / 2;
         }
+        const int s = li % C::STAGES;
+        const uint32_t ph = (li / C::STAGES) & 1;
+        if (li >= C::STAGES && !mbar_wait(bar(C::B_KVEMPTY + s), ph ^ 1, wc)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE_BYTES);
+        const CUtensorMap* m = v ? &tmV : &tmK;
+        for (int cb = 0; cb < C::CB; ++cb)
+          tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
+                      j * kBN, bh_kv);
       }
       // Drain: every issued copy must land before the CTA may exit.
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
@@ -165,64 +186,74 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       // The whole warp runs this loop (uniform operands); one elected lane issues.
-      bool ok = mbar_wait_warp(bar(C::B_QFULL), 0, wc);
-      tc_fence_after();
+      // Ring slots of the loads (see the producer): K_0 first, then K_{j+1}
+      // ahead of V_j.
+      auto k_li = [&](int j) -> int { return j == 0 ? 0 : 2 * j - 1; };
+      auto v_li = [&](int j) -> int { return j == n_kv - 1 ? 2 * n_kv - 1 : 2 * j + 2; };
       auto kv_slot = [&](int li) -> int { return li % C::STAGES; };
+      bool ok = mbar_wait_warp(bar(C::B_QFULL), 0, wc);
       auto wait_kv = [&](int li) -> bool {
         if (!mbar_wait_warp(bar(C::B_KVFULL + kv_slot(li)), (li / C::STAGES) & 1, wc)) return false;
         tc_fence_after();
         return true;
       };
-      // S_t = Q_t K^T into buffer t.
-      auto issue_s = [&](int t, int li) {
-        const uint32_t kb = sKV + kv_slot(li) * C::TILE_BYTES;
+      // S_t = Q_t K_j^T into the shared S buffer.
+      auto issue_s = [&](int t, int j) {
+        const uint32_t kb = sKV + kv_slot(k_li(j)) * C::TILE_BYTES;
         const uint32_t qb = sQ + t * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * C::BLOCK_BYTES + (kk & 3) * 32;
-          mma_ss_warp(tmem + C::TM_S + t * 128, sdesc_sw128(qb + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), C::IDESC_S, kk > 0 ? 1u : 0u);
+          mma_ss_warp(tmem + C::TM_S, sdesc_sw128(qb + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                      C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         tc_commit_warp(bar(C::B_SFULL + t));
+        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // K_j read by both tiles
       };
-      // O_t += P_t V (A = 16 keys of P = 8 TMEM columns; B = 16 V rows, MN-major).
-      auto issue_pv = [&](int t, int li, bool acc, bool last) {
-        const uint32_t vb = sKV + kv_slot(li) * C::TILE_BYTES;
+      // O_t += P_t V_j (A = 16 keys of P_t = 8 TMEM columns; B = 16 V rows, MN-major).
+      auto issue_pv = [&](int t, int j) {
+        const uint32_t vb = sKV + kv_slot(v_li(j)) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
-          mma_ts_warp(tmem + C::TM_O + t * D, tmem + C::TM_S + t * 128 + kk * 8,
+          mma_ts_warp(tmem + C::TM_O + t * D, tmem + C::TM_P + t * 64 + kk * 8,
                       sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
-                      (kk > 0 || acc) ? 1u : 0u);
-        if (last) tc_commit_warp(bar(C::B_ODONE + t));  // O_t final: one completion only
+                      (kk > 0 || j > 0) ? 1u : 0u);
+        tc_commit_warp(bar(C::B_ODONE + t));
+        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // V_j read by both tiles
       };
-      if (ok && (ok = wait_kv(0))) {
+      // The S buffer passes between the tiles: S_0(j), S_1(j), S_0(j+1), ...
+      // Each S is issued once the previous one has been read out (SFREE).
+      int sfree = 0;  // completions of SFREE waited for so far
+      auto wait_sfree = [&]() -> bool {
+        const bool r = mbar_wait_warp(bar(C::B_SFREE), sfree & 1, wc);
+        ++sfree;
+        return r;
+      };
+      if (ok) ok = wait_kv(k_li(0));
+      if (ok) {
         issue_s(0, 0);
-        issue_s(1, 0);
-        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(0)));
+        ok = wait_sfree();
       }
+      if (ok) issue_s(1, 0);
+      if (ok && n_kv > 1) ok = wait_sfree() && wait_kv(k_li(1));
+      if (ok && n_kv > 1) issue_s(0, 1);
       for (int j = 0; j < n_kv && ok; ++j) {
-        const int liK = 2 * (j + 1), liV = 2 * j + 1;
-        const bool more = j + 1 < n_kv;
-        if (!wait_kv(liV)) break;
-        for (int t = 0; t < 2; ++t) {
-          if (!mbar_wait_warp(bar(C::B_PFULL + t), j & 1, wc)) {
-            ok = false;
-            break;
-          }
+        // P_0(j) ready -> O_0 += P_0 V_j.  The S buffer then holds S_0(j+1);
+        // once tile 0 has read it, S_1(j+1) follows.
+        if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + 0), j & 1, wc)) break;
+        tc_fence_after();
+        issue_pv(0, j);
+        if (j + 1 < n_kv) {
+          if (!wait_sfree()) break;
           tc_fence_after();
-          issue_pv(t, liV, j > 0, !more);
-          if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liV)));
-          if (more) {
-            if (t == 0 && !wait_kv(liK)) {
-              ok = false;
-              break;
-            }
-            // S_t of the next tile overwrites the TMEM columns P_t V reads.
-            // tcgen05.mma operations of one CTA execute in issue order, so the
-            // reads of P_t V precede the writes of the next S_t without a wait.
-            issue_s(t, liK);
-            if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(liK)));
-          }
+          issue_s(1, j + 1);
+        }
+        if (!mbar_wait_warp(bar(C::B_PFULL + 1), j & 1, wc)) break;
+        tc_fence_after();
+        issue_pv(1, j);
+        if (j + 2 < n_kv) {
+          if (!wait_sfree() || !wait_kv(k_li(j + 2))) break;
+          issue_s(0, j + 2);
         }
       }
       // Drain: all MMAs of this warp complete before TMEM is released.
@@ -238,7 +269,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int qt0 = q0 + t * kBM;
     const int q = qt0 + row;
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
-    const uint32_t s_t = tmem + lane_off + C::TM_S + t * 128;
+    const uint32_t s_t = tmem + lane_off + C::TM_S;  // shared S buffer
+    const uint32_t p_t = tmem + lane_off + C::TM_P + t * 64;
     const uint32_t o_t = tmem + lane_off + C::TM_O + t * D;
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running (possibly stale) max of scale*s, log2 units
@@ -258,6 +290,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr[1]);
       reg_fence32(sr[2]);
       reg_fence32(sr[3]);
+      // The S buffer can take the other tile's next scores now.
+      tc_fence_before();
+      mbar_arrive(bar(C::B_SFREE));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
       if ((k0 + kBN > p.N) || (p.causal && k0 + kBN - 1 > qt0)) {
         const int lim = p.causal ? min(p.N - 1, q) : p.N - 1;
@@ -286,57 +321,57 @@ __global__ void __launch_bounds__(kThreads, 1)
         l *= alpha;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
-      if (j > 0 && __any_sync(0xffffffffu, move)) {
-        // O_t holds tiles < j: their P V precede S_t of tile j in the MMA
-        // order, and S_t of tile j has completed.
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(o_t + c * 32, o);
-          tmem_ld_wait(o);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-          tmem_st32(o_t + c * 32, o);
-        }
-      }
       // Row sums in four packed (f32x2) accumulators; x = s * scale*log2e - m
-      // for two columns per packed FMA.
+      // for two columns per packed FMA; P kept as packed bf16 pairs.
       uint64_t rs2[4] = {0, 0, 0, 0};
       const uint64_t sl2x2 = f2pack(sl2, sl2);
       const uint64_t negm2 = f2pack(-m_use, -m_use);
-      // P as packed bf16 pairs, stored in two halves of 32 TMEM columns: the
-      // first half lands on S columns [0, 32), already read into registers.
+      uint32_t w[2][32];
 #pragma unroll
-      for (int half = 0; half < 2; ++half) {
-        uint32_t w[32];
+      for (int c = 0; c < 4; ++c)
 #pragma unroll
-        for (int cc = 0; cc < 2; ++cc) {
-          const int c = 2 * half + cc;
-#pragma unroll
-          for (int i = 0; i < 16; ++i) {
-            float x0, x1;
-            f2unpack(ffma2(f2pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2,
-                           negm2),
-                     x0, x1);
-            const float p0 = ex2(x0);
-            const float p1 = ex2(x1);
-            rs2[i & 3] = fadd2(rs2[i & 3], f2pack(p0, p1));
-            w[cc * 16 + i] = pack_bf16(p0, p1);
-          }
+        for (int i = 0; i < 16; ++i) {
+          float x0, x1;
+          f2unpack(ffma2(f2pack(__uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1])), sl2x2, negm2),
+                   x0, x1);
+          const float p0 = ex2(x0);
+          const float p1 = ex2(x1);
+          rs2[i & 3] = fadd2(rs2[i & 3], f2pack(p0, p1));
+          w[c >> 1][(c & 1) * 16 + i] = pack_bf16(p0, p1);
         }
-        tmem_st32(s_t + half * 32, w);
-      }
       {
         float a0, a1;
         f2unpack(fadd2(fadd2(rs2[0], rs2[1]), fadd2(rs2[2], rs2[3])), a0, a1);
         l += a0 + a1;
       }
+      if (j > 0) {
+        // P_t V of the previous tile must be complete: it reads the P_t
+        // columns written below, and O_t may be rescaled.
+        if (!mbar_wait(bar(C::B_ODONE + t), (j - 1) & 1, wc)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        if (__any_sync(0xffffffffu, move)) {
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(o_t + c * 32, o);
+            tmem_ld_wait(o);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
+            tmem_st32(o_t + c * 32, o);
+          }
+        }
+      }
+      tmem_st32(p_t, w[0]);
+      tmem_st32(p_t + 32, w[1]);
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(bar(C::B_PFULL + t));
     }
     // Epilogue: O / l and LSE.
-    if (ok && mbar_wait(bar(C::B_ODONE + t), 0, wc)) {
+    if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
       tc_fence_after();
       const float inv_l = l > 0.f ? 1.f / l : 0.f;
       const bool valid = q < p.N;
