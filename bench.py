@@ -49,6 +49,9 @@ def parse_args(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="named workload (c3 is the benchmark; c2, c4, c5 for the table; "
+                         "c1 is fp32 forward-only and not benchmarked)")
     return ap.parse_args(argv)
 
 
@@ -204,7 +207,7 @@ def run_reference(args):
     if rank != 0:
         return 0
     from exact_attention_95_gb300 import inputs
-    w = inputs.WORKLOADS[WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
     t64 = oracle_tensors(w)
     steps, warm = max(1, args.steps), max(0, args.warmup)
     per_step = min(30.0, 150.0 / (steps + warm))
@@ -218,7 +221,7 @@ def run_reference(args):
         tot_f += fl
     value = tot_f / tot_t / 1e12
     sample = (f"fp64 oracle forward+backward of the causal prefix of {n} tokens of one head "
-              f"per step (head index = step), from the {WORKLOAD} workload tensors")
+              f"per step (head index = step), from the {args.workload} workload tensors")
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": steps,
         "warmup": warm, "ms_per_step": 1e3 * tot_t / steps, "higher_is_better": True,
@@ -232,11 +235,24 @@ def run_reference(args):
     return 0
 
 
+def working_set_bytes(w):
+    """Bytes a step touches: Q, O, dO, dQ (bf16), K, V, dK, dV, the fp32 dQ accumulator."""
+    q = w.B * w.Hq * w.N * w.d
+    kv = w.B * w.Hkv * w.N * w.d
+    return 2 * (4 * q + 4 * kv) + 4 * q
+
+
+def needs_l2_flush(w):
+    return working_set_bytes(w) < 2 * L2_BYTES
+
+
 def workload_config(w):
+    ws = working_set_bytes(w) / 2 ** 20
+    l2 = (f"working set {ws:.0f} MiB < 2x L2: L2 flushed (256 MiB write) before every timed step, "
+          "outside the step's events" if needs_l2_flush(w)
+          else f"working set {ws:.0f} MiB larger than the 126 MiB L2; no flush")
     return {"workload": w.name, "B": w.B, "Hq": w.Hq, "Hkv": w.Hkv, "N": w.N, "d": w.d,
-            "causal": w.causal, "q_scale": w.q_mul, "scale": w.scale,
-            "l2": "inputs larger than L2 (Q,K,V,dO,O 64 MiB each + 128 MiB dQ accumulator "
-                  "vs 126 MiB L2); no flush"}
+            "causal": w.causal, "q_scale": w.q_mul, "scale": w.scale, "l2": l2}
 
 
 # ---------------------------------------------------------------- native arm
@@ -252,7 +268,9 @@ def run_native(args):
     from exact_attention_95_gb300 import inputs
 
     pkg.load_library()
-    w = inputs.WORKLOADS[WORKLOAD]
+    w = inputs.WORKLOADS[args.workload]
+    if w.dtype != "bf16" or not w.backward:
+        raise SystemExit(f"{args.workload} has no bf16 forward+backward step to benchmark")
     t_np = inputs.workload_tensors(w)
 
     def dev_bf16(a):
@@ -292,6 +310,7 @@ def run_native(args):
 
     K_steps = args.steps
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K_steps)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if needs_l2_flush(w) else None
     barrier()
     torch.cuda.synchronize()
     props = torch.cuda.get_device_properties(dev)
@@ -300,6 +319,8 @@ def run_native(args):
     with ClockSampler(gpu_id) as clk:
         wall0 = time.perf_counter()
         for i in range(K_steps):
+            if flush is not None:
+                flush.zero_()
             step(evs[i])
         torch.cuda.synchronize()
         wall = time.perf_counter() - wall0
@@ -307,7 +328,9 @@ def run_native(args):
     st = pkg.attn_last_device_status()
     if st != pkg.ATTN_OK:
         raise RuntimeError(f"device status {pkg.attn_status_string(st)} in the timed region")
-    total_ms = evs[0][0].elapsed_time(evs[-1][4])
+    # Sum of the steps' own event spans (equal to the whole span when no flush
+    # runs between steps).
+    total_ms = sum(e[0].elapsed_time(e[4]) for e in evs)
     fwd_ms = [e[0].elapsed_time(e[1]) for e in evs]
     pre_ms = [e[1].elapsed_time(e[2]) for e in evs]
     main_ms = [e[2].elapsed_time(e[3]) for e in evs]
@@ -331,7 +354,7 @@ def run_native(args):
         dom, dom_tf = "bwd_main_kernel (attn_bwd_main)", main_tf
     else:
         dom, dom_tf = "fwd_bf16_kernel (attn_fwd)", fwd_tf
-    traffic = load_traffic(dom)
+    traffic = load_traffic(dom, args.workload)
     roofline = {"bound": "tensor", "achieved": dom_tf, "peak": sustained, "unit": "TFLOP/s",
                 "frac": dom_tf / sustained, "traffic": traffic, "kernel": dom,
                 "peak_source": f"bf16_tflops_sustained of {peak_src}"}
@@ -374,9 +397,10 @@ def kernel_source_sha(kernel_file):
     return h.hexdigest()
 
 
-def load_traffic(kernel_desc):
+def load_traffic(kernel_desc, workload):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when there is none or the kernel changed since."""
+    summary, or None when there is none for this workload or the kernel
+    changed since the capture."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     try:
         with open(path) as f:
@@ -385,7 +409,7 @@ def load_traffic(kernel_desc):
         return None
     key, src = ("bwd_main", "bwd_sm103.cu") if kernel_desc.startswith("bwd_main") else ("fwd", "fwd_sm103.cu")
     ent = d.get(key)
-    if not ent or ent.get("source_sha256") != kernel_source_sha(src):
+    if not ent or ent.get("workload") != workload or ent.get("source_sha256") != kernel_source_sha(src):
         return None
     return ent.get("bytes_per_launch")
 
@@ -451,7 +475,7 @@ def cpu_baseline(w, budget_s):
         tot_f += fl
         heads += 1
     return {"value": tot_f / tot_t / 1e12, "unit": "TFLOPS", "cores": cpu_cores(), "kind": "oracle",
-            "sample": f"fp64 oracle forward+backward of {heads} head(s) of batch 0 of {WORKLOAD}, "
+            "sample": f"fp64 oracle forward+backward of {heads} head(s) of batch 0 of {w.name.split(':')[0]}, "
                       f"causal prefix of {n} tokens each, {tot_t:.1f} s"}
 
 
