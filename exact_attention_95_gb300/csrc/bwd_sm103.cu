@@ -73,14 +73,19 @@ struct Bwd {
   static constexpr int STAGES = 2;
   static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
   static constexpr int B_KVFULL = 0;
-  static constexpr int B_STFULL = 1;  // STAGES
-  static constexpr int B_STEMPTY = B_STFULL + STAGES;
-  static constexpr int B_SFULL = B_STEMPTY + STAGES;
+  // Each stage has two halves with their own barriers: the Q part (Q tile,
+  // -LSE2, -D) and the dO part, released separately by the dQ reducer.
+  static constexpr int B_STFULL = 1;                     // STAGES: Q part landed
+  static constexpr int B_STFULL_DO = B_STFULL + STAGES;  // STAGES: dO part landed
+  static constexpr int B_STEMPTY = B_STFULL_DO + STAGES; // STAGES: Q slot free
+  static constexpr int B_STEMPTY_DO = B_STEMPTY + STAGES;  // STAGES: dO slot free
+  static constexpr int B_SFULL = B_STEMPTY_DO + STAGES;
   static constexpr int B_DPFULL = B_SFULL + 1;
   static constexpr int B_PFULL = B_DPFULL + 1;
   static constexpr int B_DVDONE = B_PFULL + 1;
-  static constexpr int B_DSFULL = B_DVDONE + 1;
-  static constexpr int B_KVDONE = B_DSFULL + 1;
+  static constexpr int B_DSTMEM = B_DVDONE + 1;  // dS in TMEM (for dK)
+  static constexpr int B_DSSMEM = B_DSTMEM + 1;  // dS in shared memory (for dQ)
+  static constexpr int B_KVDONE = B_DSSMEM + 1;
   static constexpr int B_DQFULL = B_KVDONE + 1;
   static constexpr int B_DQFREE = B_DQFULL + 1;
   static constexpr int B_DQSTAGED = B_DQFREE + 1;  // 2: one per math warpgroup
@@ -161,6 +166,35 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
 }
 
 // ------------------------------------------------------------------ main
+// P = 2^(s * scale * log2e - LSE2) for the 64 query columns of one math
+// warpgroup, two columns per packed FMA (the workspace holds -LSE2): fp32 pairs
+// into pv2 (for dS) and bf16 pairs into pk (the dV operand).  With MASK,
+// columns c < cmin are zero (keys after the query on a diagonal tile, or a key
+// row past N); other tiles skip the per-element test.
+template <bool MASK>
+__device__ __forceinline__ void bwd_probs(const uint32_t (&sr)[2][32], uint32_t lse_addr, float sl2, int cmin,
+                                          uint64_t (&pv2)[32], uint32_t (&pk)[32]) {
+  const uint64_t sl2x2 = f2pack(sl2, sl2);
+#pragma unroll
+  for (int c4 = 0; c4 < 16; ++c4) {
+    const float4 nl = lds_f4(lse_addr + 16 * c4);  // same address in all lanes
+#pragma unroll
+    for (int u = 0; u < 2; ++u) {
+      const int c = 4 * c4 + 2 * u;
+      const uint64_t s2 = f2pack(__uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]));
+      float x0, x1;
+      f2unpack(ffma2(s2, sl2x2, u == 0 ? f2pack(nl.x, nl.y) : f2pack(nl.z, nl.w)), x0, x1);
+      float p0 = ex2(x0), p1 = ex2(x1);
+      if (MASK) {
+        if (c < cmin) p0 = 0.f;
+        if (c + 1 < cmin) p1 = 0.f;
+      }
+      pv2[c / 2] = f2pack(p0, p1);
+      pk[c / 2] = pack_bf16(p0, p1);
+    }
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
@@ -197,13 +231,16 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(bar(C::B_KVFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_STFULL + s), 1);
-      mbar_init(bar(C::B_STEMPTY + s), 1);  // arrived by the dQ reducer
+      mbar_init(bar(C::B_STFULL_DO + s), 1);
+      mbar_init(bar(C::B_STEMPTY + s), 1);     // arrived by the dQ reducer
+      mbar_init(bar(C::B_STEMPTY_DO + s), 1);  // arrived by the dQ reducer
     }
     mbar_init(bar(C::B_SFULL), 1);
     mbar_init(bar(C::B_DPFULL), 1);
     mbar_init(bar(C::B_PFULL), 256);
     mbar_init(bar(C::B_DVDONE), 1);
-    mbar_init(bar(C::B_DSFULL), 256);
+    mbar_init(bar(C::B_DSTMEM), 256);
+    mbar_init(bar(C::B_DSSMEM), 256);
     mbar_init(bar(C::B_KVDONE), 1);
     mbar_init(bar(C::B_DQFULL), 1);
     mbar_init(bar(C::B_DQFREE), 256);
@@ -236,8 +273,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tma_load_3d(sK + cb * C::BLK, &tmK, bar(C::B_KVFULL), cb * 64, k0, bhk);
         tma_load_3d(sV + cb * C::BLK, &tmV, bar(C::B_KVFULL), cb * 64, k0, bhk);
       }
-      int t = 0;
-      for (; t < T; ++t) {
+      int tq = 0, tdo = 0;  // Q parts and dO parts issued
+      for (int t = 0; t < T; ++t) {
         const int s = t % C::STAGES;
         if (t >= C::STAGES && !mbar_wait(bar(C::B_STEMPTY + s), ((t / C::STAGES) & 1) ^ 1, wc)) break;
         const int g = t / per_head;
@@ -245,11 +282,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int bhq = b * p.Hq + hk * G + g;
         const uint32_t st = stage(s);
         const uint32_t fb = bar(C::B_STFULL + s);
-        mbar_arrive_expect_tx(fb, 2 * C::CB * C::BLK + 2 * kBQ * 4);
-        for (int cb = 0; cb < C::CB; ++cb) {
+        mbar_arrive_expect_tx(fb, C::CB * C::BLK + 2 * kBQ * 4);
+        for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(st + C::ST_Q + cb * C::BLK, &tmQ, fb, cb * 64, it * kBQ, bhq);
-          tma_load_3d(st + C::ST_DO + cb * C::BLK, &tmdO, fb, cb * 64, it * kBQ, bhq);
-        }
         const size_t vo = (size_t)bhq * p.Npad + (size_t)it * kBQ;
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
@@ -261,10 +296,20 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                 st + C::ST_D),
             "l"(p.negD + vo), "r"(kBQ * 4), "r"(fb)
             : "memory");
+        tq = t + 1;
+        if (t >= C::STAGES && !mbar_wait(bar(C::B_STEMPTY_DO + s), ((t / C::STAGES) & 1) ^ 1, wc)) break;
+        const uint32_t fbd = bar(C::B_STFULL_DO + s);
+        mbar_arrive_expect_tx(fbd, C::CB * C::BLK);
+        for (int cb = 0; cb < C::CB; ++cb)
+          tma_load_3d(st + C::ST_DO + cb * C::BLK, &tmdO, fbd, cb * 64, it * kBQ, bhq);
+        tdo = t + 1;
       }
+      // Before exiting, wait for the copies this thread may still have in flight.
       mbar_wait_drain(bar(C::B_KVFULL), 0, wc);
-      for (int k = max(0, t - C::STAGES); k < t; ++k)
+      for (int k = max(0, tq - C::STAGES); k < tq; ++k)
         mbar_wait_drain(bar(C::B_STFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
+      for (int k = max(0, tdo - C::STAGES); k < tdo; ++k)
+        mbar_wait_drain(bar(C::B_STFULL_DO + k % C::STAGES), (k / C::STAGES) & 1, wc);
     } else if (warp == 1) {
       // ---------------------------------------------------------- MMA issuer
       // The whole warp runs this loop (uniform operands); one elected lane issues.
@@ -287,6 +332,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tc_commit_warp(bar(C::B_SFULL));
         // Region DP is free once the previous dQ^T has been read back.
         if (t > 0 && !mbar_wait_warp(bar(C::B_DQFREE), (t - 1) & 1, wc)) break;
+        if (!mbar_wait_warp(bar(C::B_STFULL_DO + s), (t / C::STAGES) & 1, wc)) break;
         tc_fence_after();
         // dP^T = V dO^T.
 #pragma unroll
@@ -307,7 +353,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                       (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_DVDONE));
         // dK += dS^T Q (dS in region S columns [64h+32, 64h+64)).
-        if (!mbar_wait_warp(bar(C::B_DSFULL), t & 1, wc)) break;
+        if (!mbar_wait_warp(bar(C::B_DSTMEM), t & 1, wc)) break;
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kBQ / 16; ++kk)
@@ -315,6 +361,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                       sdesc_sw128(qs + kk * 2048, C::BLK, 1024), C::IDESC_KV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_KVDONE));
+        if (!mbar_wait_warp(bar(C::B_DSSMEM), t & 1, wc)) break;
+        tc_fence_after();
         // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS^T in the dO
         // slot, MN-major [keys x queries] (two 64-query blocks).  For d = 64
         // the product still has M = 128; lanes 64..127 read the V tile as
@@ -345,11 +393,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
           }
           tma_reduce_add_2d(&tmDQ, st + (h == 0 ? C::ST_Q : C::ST_DO), 0,
                             (int)((size_t)bhq * p.Npad + (size_t)it * kBQ + 64 * h));
+          bulk_commit_group();
         }
-        bulk_commit_group();
         if (!ok) break;
-        bulk_wait_read0();
+        bulk_wait_read1();  // the first half (Q slot) has been read
         mbar_arrive(bar(C::B_STEMPTY + s));
+        bulk_wait_read0();
+        mbar_arrive(bar(C::B_STEMPTY_DO + s));
       }
       bulk_wait0();
     }
@@ -380,32 +430,21 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         break;
       }
       tc_fence_after();
-      // ---- P = 2^(s * scale * log2e - LSE2) for 64 query columns, two per
-      // packed FMA (the workspace holds -LSE2).
+      // ---- P for this warpgroup's 64 query columns.
       uint32_t sr[2][32];
       tmem_ld32(tS, sr[0]);
       tmem_ld32(tS + 32, sr[1]);
       tmem_ld_wait(sr[0]);
       reg_fence32(sr[1]);
-      const bool diag = p.causal && (qh0 < k0 + kBK - 1);
-      const uint64_t sl2x2 = f2pack(sl2, sl2);
       uint64_t pv2[32];  // P, column pairs
       uint32_t pk[32];
-#pragma unroll
-      for (int c4 = 0; c4 < 16; ++c4) {
-        const float4 nl = lds_f4(st + C::ST_LSE + 4 * (64 * h + 4 * c4));  // same address in all lanes
-#pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int c = 4 * c4 + 2 * u;
-          const uint64_t s2 = f2pack(__uint_as_float(sr[c >> 5][c & 31]), __uint_as_float(sr[c >> 5][(c & 31) + 1]));
-          float x0, x1;
-          f2unpack(ffma2(s2, sl2x2, u == 0 ? f2pack(nl.x, nl.y) : f2pack(nl.z, nl.w)), x0, x1);
-          float p0 = ex2(x0), p1 = ex2(x1);
-          if (!key_ok || (diag && key > qh0 + c)) p0 = 0.f;
-          if (!key_ok || (diag && key > qh0 + c + 1)) p1 = 0.f;
-          pv2[c / 2] = f2pack(p0, p1);
-          pk[c / 2] = pack_bf16(p0, p1);
-        }
+      const uint32_t lse_addr = st + C::ST_LSE + 4 * 64 * h;
+      // Tile-uniform test: a ragged key tile, or a causal tile that crosses the diagonal.
+      if (k0 + kBK > p.N || (p.causal && qh0 < k0 + kBK - 1)) {
+        const int cmin = !key_ok ? 64 : (p.causal ? max(0, key - qh0) : 0);
+        bwd_probs<true>(sr, lse_addr, sl2, cmin, pv2, pk);
+      } else {
+        bwd_probs<false>(sr, lse_addr, sl2, 0, pv2, pk);
       }
       tmem_st32(tS, pk);
       tmem_st_wait();
@@ -437,6 +476,9 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         }
       }
       tmem_st32(tS + 32, pk);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(bar(C::B_DSTMEM));
       // dS^T rows into the dO slot (dV, its last reader, must be complete):
       // block h holds query columns [64h, 64h+64); row kr is 128 bytes with
       // the 16-byte chunk c stored at chunk position c ^ (kr & 7).
@@ -449,9 +491,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int c = 0; c < 8; ++c)
         sts_u4(dsrow + ((c ^ (kr & 7)) << 4), pk[4 * c], pk[4 * c + 1], pk[4 * c + 2], pk[4 * c + 3]);
       fence_async_smem();
-      tmem_st_wait();
-      tc_fence_before();
-      mbar_arrive(bar(C::B_DSFULL));
+      mbar_arrive(bar(C::B_DSSMEM));
       // ---- dQ^T readback: 64 query columns of head-dim row dcol.
       if (!mbar_wait(bar(C::B_DQFULL), t & 1, wc)) {
         ok = false;

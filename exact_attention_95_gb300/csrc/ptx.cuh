@@ -415,3 +415,13 @@ __device__ __forceinline__ uint64_t fmul2(uint64_t a, uint64_t b) {
 }
 
 }  // namespace attn
+
+namespace attn {
+
+// Wait until all but the most recent bulk group of this thread have finished
+// reading shared memory.
+__device__ __forceinline__ void bulk_wait_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
+}  // namespace attn
