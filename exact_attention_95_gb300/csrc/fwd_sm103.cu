@@ -13,8 +13,8 @@
 // The running max may lag behind the true max: softmax(s) = e^{s-m} / sum e^{s-m}
 // holds for any m (§5.1 of the same notes), so a row only moves its m (and
 // rescales l and its O row) when the new tile's max exceeds it by more than
-// 2^8; otherwise P~ = 2^{s - m} <= 256, which bf16 P and fp32 l, O hold as
-// well as values <= 1.
+// 2^16; otherwise P~ = 2^{s - m} <= 65536, which bf16 P (8 exponent bits) and
+// fp32 l, O hold with the same relative precision as values <= 1.
 //
 // Mapping to the hardware (one CTA = two 128-row query tiles, 12 warps):
 //   warp 0      TMA producer: both Q tiles once, then K and V tiles through a
@@ -51,7 +51,7 @@ constexpr int kRegsHigh = 216;    // softmax warpgroups after setmaxnreg.inc
 static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
-constexpr float kRescaleThreshold = 8.0f;  // log2 units: rescale when m grows by > 2^8
+constexpr float kRescaleThreshold = 16.0f;  // log2 units: rescale when m grows by > 2^16
 
 template <int D>
 struct Fwd {
@@ -117,10 +117,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::B_SFULL + i), 1);
-      mbar_init(bar(C::B_PFULL + i), kBM);
+      mbar_init(bar(C::B_PFULL + i), 4);  // one arrival per softmax warp
       mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_SFREE), kBM);
+    mbar_init(bar(C::B_SFREE), 4);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -274,7 +274,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t o_t = tmem + lane_off + C::TM_O + t * D;
     const float sl2 = p.scale_log2;
     float m = -INFINITY;  // running (possibly stale) max of scale*s, log2 units
-    float l = 0.f;        // running sum of 2^(scale*s*log2e - m)
+    float l = 0.f;        // running sum of 2^(scale*s*log2e - m): gives LSE
+    float corr = 0.f;     // sum over tiles of (largest P - its bf16 rounding), same scale as l
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
       const int k0 = j * kBN;
@@ -292,7 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr[3]);
       // The S buffer can take the other tile's next scores now.
       tc_fence_before();
-      mbar_arrive(bar(C::B_SFREE));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_SFREE));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
       if ((k0 + kBN > p.N) || (p.causal && k0 + kBN - 1 > qt0)) {
         const int lim = p.causal ? min(p.N - 1, q) : p.N - 1;
@@ -310,8 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int i = 0; i < 16; ++i)
           mp[i & 7] = fmax3(mp[i & 7], __uint_as_float(sr[c][2 * i]), __uint_as_float(sr[c][2 * i + 1]));
-      const float mx = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
-                             fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7]))) * sl2;
+      const float mraw = fmaxf(fmaxf(fmaxf(mp[0], mp[1]), fmaxf(mp[2], mp[3])),
+                               fmaxf(fmaxf(mp[4], mp[5]), fmaxf(mp[6], mp[7])));
+      const float mx = mraw * sl2;
       // Move m only when the tile's max exceeds it by more than the threshold.
       const bool move = mx > m + kRescaleThreshold;
       float alpha = 1.f;
@@ -319,8 +322,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         alpha = ex2(m - mx);  // 0 when m = -inf
         m = mx;
         l *= alpha;
+        corr *= alpha;
       }
       const float m_use = (m == -INFINITY) ? 0.f : m;
+      {
+        // The tile's largest P as the loop below computes it, and what its
+        // rounding to bf16 (the P that multiplies V) takes away from it.
+        const float pmax = ex2(fmaf(mraw, sl2, -m_use));
+        corr += pmax - __uint_as_float(pack_bf16(pmax, pmax) & 0xffff0000u);
+      }
       // Row sums in four packed (f32x2) accumulators; x = s * scale*log2e - m
       // for two columns per packed FMA; P kept as packed bf16 pairs.
       uint64_t rs2[4] = {0, 0, 0, 0};
@@ -353,14 +363,17 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         tc_fence_after();
         if (__any_sync(0xffffffffu, move)) {
+          // The whole O row in one round trip (sr is free again).
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) tmem_ld32(o_t + c * 32, sr[c]);
+          tmem_ld_wait(sr[0]);
+#pragma unroll
+          for (int c = 1; c < D / 32; ++c) reg_fence32(sr[c]);
 #pragma unroll
           for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(o_t + c * 32, o);
-            tmem_ld_wait(o);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o[i] = __float_as_uint(__uint_as_float(o[i]) * alpha);
-            tmem_st32(o_t + c * 32, o);
+            for (int i = 0; i < 32; ++i) sr[c][i] = __float_as_uint(__uint_as_float(sr[c][i]) * alpha);
+            tmem_st32(o_t + c * 32, sr[c]);
           }
         }
       }
@@ -368,12 +381,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       tmem_st32(p_t + 32, w[1]);
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(bar(C::B_PFULL + t));
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
     }
     // Epilogue: O / l and LSE.
     if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
       tc_fence_after();
-      const float inv_l = l > 0.f ? 1.f / l : 0.f;
+      // O is divided by the row sum less the rounding of each tile's largest
+      // P: when one key dominates a row, its bf16 rounding then cancels
+      // between O and the divisor.  LSE uses the exact sum.
+      const float lo = l - corr;
+      const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
       const bool valid = q < p.N;
       const size_t row_idx = (size_t)bh * p.N + q;
 #pragma unroll

@@ -67,6 +67,33 @@ def test_fwd_bf16_out_and_large_logits(causal):
     assert np.abs(L - Lref).max() <= LSE_TOL
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_fwd_rescale_path(causal):
+    # Key rows scaled up along the sequence (x0.25 .. x2.5) with Q x8: every
+    # row's running max keeps growing by far more than the 2^16 the kernel
+    # tolerates before it rescales O and l, so the rescale runs on many tiles.
+    B, Hq, Hkv, N, d = 1, 2, 1, 1536, 128
+    t = make(B, Hq, Hkv, N, d, 4242, q_mul=8.0, names=("Q", "K", "V"))
+    ramp = np.linspace(0.25, 2.5, N)[None, None, :, None]
+    t["K"] = inputs.round_to_bf16_bits(inputs.to_f64(t["K"]) * ramp)
+    g = {k: to_dev(v) for k, v in t.items()}
+    scale = 1.0 / np.sqrt(d)
+    O, L = pkg.attn_fwd(g["Q"], g["K"], g["V"], scale, causal, out_dtype=torch.float32)
+    torch.cuda.synchronize()
+    assert pkg.attn_last_device_status() == pkg.ATTN_OK
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    Oref, Lref = oracle.fwd(f["Q"], f["K"], f["V"], scale, causal)
+    # The growth is real: the row max over the last tile exceeds the one over
+    # the first tile by more than 16 in log2 units for most rows.
+    s = np.einsum("bhnd,bhmd->bhnm", f["Q"][:, :1, -128:], f["K"][:, :, :128]) * scale
+    s_last = np.einsum("bhnd,bhmd->bhnm", f["Q"][:, :1, -128:], f["K"][:, :, -128:]) * scale
+    grow = (s_last.max(-1) - s.max(-1)) / np.log(2.0)
+    assert np.mean(grow > 16) > 0.5
+    err_o, ok = check_o(f64(O), Oref, bf16_out=False)
+    assert ok, f"O max-abs {err_o:.3e}"
+    assert np.abs(f64(L) - Lref).max() <= LSE_TOL
+
+
 def test_fwd_is_deterministic():
     t = make(1, 4, 2, 513, 128, 5, names=("Q", "K", "V"))
     g = {k: to_dev(v) for k, v in t.items()}
