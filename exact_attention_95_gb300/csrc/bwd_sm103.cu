@@ -41,6 +41,8 @@
 // reader of dO) has completed.
 #include <algorithm>
 
+#include <type_traits>
+
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -105,63 +107,97 @@ struct Bwd {
 };
 
 // ------------------------------------------------------------------ preprocess
-// One warp per (b, h, row) of the padded row range: -D, -LSE * log2(e), and a
-// zeroed accumulator row.  Rows past N get D = 0 and -LSE2 = -inf (probability 0).
+// One warp per four consecutive rows of the padded row range (four rows never
+// straddle two heads: Npad is a multiple of 128): -D, -LSE * log2(e), and
+// zeroed accumulator rows.  Rows past N get D = 0 and -LSE2 = -inf
+// (probability 0).  All loads of the four rows are issued before any use, so
+// each warp keeps 4 x 2 row reads in flight.
+constexpr int kRowsPerWarp = 4;
 template <int D>
 __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
   constexpr int EPL = D / 32;  // elements per lane
-  const long long rows = (long long)p.B * p.Hq * p.Npad;
+  using Vec = typename std::conditional<EPL == 4, uint2, uint32_t>::type;
+  const long long chunks = (long long)p.B * p.Hq * p.Npad / kRowsPerWarp;
   const int lane = threadIdx.x & 31;
-  for (long long r = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; r < rows;
-       r += ((long long)gridDim.x * blockDim.x) >> 5) {
-    const long long bh = r / p.Npad;
-    const int i = (int)(r - bh * p.Npad);
-    float dsum = 0.f;
-    if (i < p.N) {
-      const size_t off = ((size_t)bh * p.N + i) * D + lane * EPL;
-      if (EPL == 4) {
-        const uint2 a = *reinterpret_cast<const uint2*>(p.O + off);
-        const uint2 g = *reinterpret_cast<const uint2*>(p.dO + off);
-        const uint32_t aw[2] = {a.x, a.y}, gw[2] = {g.x, g.y};
+  for (long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < chunks;
+       c += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const long long r0 = c * kRowsPerWarp;
+    const long long bh = r0 / p.Npad;
+    const int i0 = (int)(r0 - bh * p.Npad);
+    Vec a[kRowsPerWarp], g[kRowsPerWarp];
 #pragma unroll
-        for (int k = 0; k < 2; ++k) {
-          dsum += __uint_as_float(aw[k] << 16) * __uint_as_float(gw[k] << 16);
-          dsum += __uint_as_float(aw[k] & 0xffff0000u) * __uint_as_float(gw[k] & 0xffff0000u);
-        }
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      if (i0 + u < p.N) {
+        const size_t off = ((size_t)bh * p.N + i0 + u) * D + lane * EPL;
+        a[u] = *reinterpret_cast<const Vec*>(p.O + off);
+        g[u] = *reinterpret_cast<const Vec*>(p.dO + off);
       } else {
-        const uint32_t a = *reinterpret_cast<const uint32_t*>(p.O + off);
-        const uint32_t g = *reinterpret_cast<const uint32_t*>(p.dO + off);
-        dsum += __uint_as_float(a << 16) * __uint_as_float(g << 16);
-        dsum += __uint_as_float(a & 0xffff0000u) * __uint_as_float(g & 0xffff0000u);
+        a[u] = Vec{};
+        g[u] = Vec{};
       }
     }
+    // Lane u < 4 fetches the LSE of row u.
+    float lse = 0.f;
+    if (lane < kRowsPerWarp && i0 + lane < p.N) lse = p.LSE[bh * p.N + i0 + lane];
+    float dsum[kRowsPerWarp];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) dsum += __shfl_xor_sync(0xffffffffu, dsum, o);
-    if (lane == 0) {
-      p.negD[r] = -dsum;
-      p.negLSE2[r] = i < p.N ? -p.LSE[bh * p.N + i] * 1.4426950408889634f : -INFINITY;
+    for (int u = 0; u < kRowsPerWarp; ++u) {
+      const uint32_t* aw = reinterpret_cast<const uint32_t*>(&a[u]);
+      const uint32_t* gw = reinterpret_cast<const uint32_t*>(&g[u]);
+      float sum = 0.f;
+#pragma unroll
+      for (int k = 0; k < EPL / 2; ++k) {
+        sum += __uint_as_float(aw[k] << 16) * __uint_as_float(gw[k] << 16);
+        sum += __uint_as_float(aw[k] & 0xffff0000u) * __uint_as_float(gw[k] & 0xffff0000u);
+      }
+      dsum[u] = sum;
     }
-    float4* acc = reinterpret_cast<float4*>(p.dQacc + r * D);
-    for (int k = lane; k < D / 4; k += 32) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+#pragma unroll
+      for (int u = 0; u < kRowsPerWarp; ++u) dsum[u] += __shfl_xor_sync(0xffffffffu, dsum[u], o);
+    if (lane < kRowsPerWarp) {
+      float mine = dsum[0];
+#pragma unroll
+      for (int u = 1; u < kRowsPerWarp; ++u)
+        if (lane == u) mine = dsum[u];
+      p.negD[r0 + lane] = -mine;
+      p.negLSE2[r0 + lane] = i0 + lane < p.N ? -lse * 1.4426950408889634f : -INFINITY;
+    }
+    float4* acc = reinterpret_cast<float4*>(p.dQacc + r0 * D);
+    for (int k = lane; k < kRowsPerWarp * D / 4; k += 32) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
 }
 
 // ------------------------------------------------------------------ dQ convert
+// dQ = bf16(scale * accumulator): one warp per four consecutive padded rows of
+// one head, all four rows' loads issued first.
 template <int D>
 __global__ void __launch_bounds__(256) bwd_dq_kernel(const BwdParams p) {
-  const long long total = (long long)p.B * p.Hq * p.N * (D / 4);
-  for (long long v = (long long)blockIdx.x * blockDim.x + threadIdx.x; v < total;
-       v += (long long)gridDim.x * blockDim.x) {
-    const long long e = v * 4;
-    const long long row = e / D;  // (b*Hq + h) * N + i
-    const int col = (int)(e - row * D);
-    const long long bh = row / p.N;
-    const long long i = row - bh * p.N;
-    const float4 a = *reinterpret_cast<const float4*>(p.dQacc + (bh * p.Npad + i) * D + col);
-    uint2 o;
-    o.x = pack_bf16(a.x * p.scale, a.y * p.scale);
-    o.y = pack_bf16(a.z * p.scale, a.w * p.scale);
-    *reinterpret_cast<uint2*>(p.dQ + row * D + col) = o;
+  constexpr int V4 = D / 4;  // float4 per row
+  const long long chunks = (long long)p.B * p.Hq * p.Npad / kRowsPerWarp;
+  const int lane = threadIdx.x & 31;
+  for (long long c = ((long long)blockIdx.x * blockDim.x + threadIdx.x) >> 5; c < chunks;
+       c += ((long long)gridDim.x * blockDim.x) >> 5) {
+    const long long r0 = c * kRowsPerWarp;
+    const long long bh = r0 / p.Npad;
+    const int i0 = (int)(r0 - bh * p.Npad);
+    const float4* src = reinterpret_cast<const float4*>(p.dQacc + r0 * D);
+    constexpr int PER_LANE = kRowsPerWarp * V4 / 32;
+    float4 v[PER_LANE];
+#pragma unroll
+    for (int k = 0; k < PER_LANE; ++k) v[k] = src[lane + 32 * k];
+#pragma unroll
+    for (int k = 0; k < PER_LANE; ++k) {
+      const int e = lane + 32 * k;  // float4 index within the four rows
+      const int u = e / V4, col = (e - u * V4) * 4;
+      if (i0 + u < p.N) {
+        uint2 o;
+        o.x = pack_bf16(v[k].x * p.scale, v[k].y * p.scale);
+        o.y = pack_bf16(v[k].z * p.scale, v[k].w * p.scale);
+        *reinterpret_cast<uint2*>(p.dQ + ((size_t)bh * p.N + i0 + u) * D + col) = o;
+      }
+    }
   }
 }
 
@@ -568,8 +604,8 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaError_t e = cudaSuccess;
   if (stages & kBwdPre) {
-    const long long rows = (long long)p.B * p.Hq * p.Npad;
-    const int pre_blocks = (int)std::min<long long>((rows + 7) / 8, (long long)sms * 16);
+    const long long warps = (long long)p.B * p.Hq * p.Npad / kRowsPerWarp;
+    const int pre_blocks = (int)std::min<long long>((warps + 7) / 8, (long long)sms * 8);
     bwd_pre_kernel<D><<<pre_blocks, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
@@ -591,8 +627,8 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & kBwdConvert) {
-    const long long vec = (long long)p.B * p.Hq * p.N * (D / 4);
-    const int cv_blocks = (int)std::min<long long>((vec + 255) / 256, (long long)sms * 16);
+    const long long warps = (long long)p.B * p.Hq * p.Npad / kRowsPerWarp;
+    const int cv_blocks = (int)std::min<long long>((warps + 7) / 8, (long long)sms * 8);
     bwd_dq_kernel<D><<<cv_blocks, 256, 0, stream>>>(p);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
