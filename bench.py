@@ -51,7 +51,7 @@ def parse_args(argv=None):
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="named workload (c3 is the benchmark; c2, c4, c5 for the table; "
-                         "c1 is fp32 forward-only and not benchmarked)")
+                         "c1 times the fp32 forward only)")
     return ap.parse_args(argv)
 
 
@@ -270,7 +270,7 @@ def run_native(args):
     pkg.load_library()
     w = inputs.WORKLOADS[args.workload]
     if w.dtype != "bf16" or not w.backward:
-        raise SystemExit(f"{args.workload} has no bf16 forward+backward step to benchmark")
+        return run_fwd_only(args, w, pkg, rank, world, dev)
     t_np = inputs.workload_tensors(w)
 
     def dev_bf16(a):
@@ -360,6 +360,13 @@ def run_native(args):
                 "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
     e2e = run_e2e(args, pkg, w, t_np, dev, stream, ffl + bfl, world)
+    # The secondary ceiling: one exponential per kept score, in the forward
+    # and again in the backward's recomputation of P.
+    n_exp = exp_count(w)
+    sfu = sfu_peak_per_s(props, peaks)
+    exps = {"per_launch": n_exp, "fwd_per_s": n_exp / (fwd_avg / 1e3),
+            "bwd_main_per_s": n_exp / (main_avg / 1e3), "sfu_peak_per_s": sfu,
+            "fwd_frac": n_exp / (fwd_avg / 1e3) / sfu}
 
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K_steps,
@@ -374,6 +381,7 @@ def run_native(args):
                 "ms_preprocess": statistics.mean(pre_ms), "ms_main": main_avg,
                 "ms_convert": statistics.mean(cv_ms)},
         "roofline": roofline,
+        "exp": exps,
         "e2e": e2e,
         "gpu_launches": launches_per_step * K_steps,
         "clocks": clocks,
@@ -384,6 +392,130 @@ def run_native(args):
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0
+
+
+def exp_count(w):
+    """Kept scores per launch (one exponential each): N^2 per head, N(N+1)/2
+    when causal."""
+    per_head = w.N * (w.N + 1) / 2 if w.causal else float(w.N) * w.N
+    return per_head * w.B * w.Hq
+
+
+def sfu_peak_per_s(props, peaks):
+    """ex2.approx.ftz.f32 throughput: 32 per clock per SM (measured on GB300)
+    at the maximum SM clock."""
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return 32.0 * props.multi_processor_count * mhz * 1e6
+
+
+def fp32_fma_peak_tflops(props, peaks):
+    """Dense fp32 FFMA peak: 128 FMA lanes per SM (4 sub-partitions x 32) x 2
+    FLOP per FMA at the maximum SM clock."""
+    mhz = float(peaks.get("sm_max_mhz", 2070.0))
+    return 256.0 * props.multi_processor_count * mhz * 1e6 / 1e12
+
+
+def run_fwd_only(args, w, pkg, rank, world, dev):
+    """Forward-only workloads (c1: the fp32 CUDA-core path).  Same timing rules
+    as the bf16 step: warm-up, CUDA events per step, L2 flushed between steps
+    (the working set is tiny), clocks sampled during the timed region."""
+    import numpy as np
+    import torch
+    from exact_attention_95_gb300 import inputs
+
+    t_np = inputs.workload_tensors(w, names=("Q", "K", "V"))
+    Q, K, V = (torch.from_numpy(np.ascontiguousarray(t_np[k])).to(dev) for k in ("Q", "K", "V"))
+    O = torch.empty_like(Q)
+    LSE = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream()
+
+    def step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        pkg.attn_fwd(Q, K, V, w.scale, w.causal, out_dtype=torch.float32, O=O, LSE=LSE, stream=stream)
+        if ev is not None:
+            ev[1].record(stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pkg.attn_last_device_status() != pkg.ATTN_OK:
+        raise RuntimeError("device status not OK after warm-up")
+    K_steps = args.steps
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(K_steps)]
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    barrier()
+    torch.cuda.synchronize()
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(dev.index)
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        for i in range(K_steps):
+            flush.zero_()
+            step(evs[i])
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - wall0
+    barrier()
+    total_ms = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in evs), dev)
+    ms = total_ms / K_steps
+    ffl = w.fwd_flops()
+    value = ffl * world / (ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    peak = fp32_fma_peak_tflops(props, peaks)
+    # e2e: H2D of Q, K, V and D2H of O through the public API, per step.
+    host = {k: torch.from_numpy(np.ascontiguousarray(t_np[k])).pin_memory() for k in ("Q", "K", "V")}
+    hO = torch.empty(O.shape, dtype=torch.float32).pin_memory()
+    e_steps = max(1, args.e2e_steps)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        Qd, Kd, Vd = (host[k].to(dev, non_blocking=True) for k in ("Q", "K", "V"))
+        Od, _ = pkg.attn_fwd(Qd, Kd, Vd, w.scale, w.causal, out_dtype=torch.float32, stream=stream)
+        hO.copy_(Od, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = max_over_ranks(e0.elapsed_time(e1), dev) / e_steps
+    in_bytes = sum(t.numel() * t.element_size() for t in host.values())
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": K_steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic (seeded iid N(0,1), fp32)",
+        "config": dict(workload_config(w), parallelism=f"replicas x{world} (weak)"),
+        "fwd": {"ms": ms, "tflops": value / world},
+        "roofline": {"bound": "alu", "achieved": value / world, "peak": peak, "unit": "TFLOP/s",
+                     "frac": value / world / peak, "traffic": None, "kernel": "fwd_f32_kernel (attn_fwd)",
+                     "peak_source": "fp32 FFMA: 128 lanes/SM x 2 FLOP x SMs x max SM clock "
+                                    f"({peak_src} clock)"},
+        "e2e": {"value": ffl * world / (e_ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": e_ms,
+                "h2d_bytes_per_step": in_bytes, "d2h_bytes_per_step": hO.numel() * 4},
+        "gpu_launches": K_steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline_fwd(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def cpu_baseline_fwd(w, budget_s):
+    """The oracle's forward on the whole (tiny) workload, repeated for about
+    budget_s seconds."""
+    import oracle
+    from exact_attention_95_gb300 import inputs
+    t = inputs.workload_tensors(w, names=("Q", "K", "V"))
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    runs, t0 = 0, time.perf_counter()
+    while time.perf_counter() - t0 < budget_s and runs < 100000:
+        oracle.fwd(f["Q"], f["K"], f["V"], w.scale, w.causal)
+        runs += 1
+    dt = time.perf_counter() - t0
+    return {"value": w.fwd_flops() * runs / dt / 1e12, "unit": "TFLOPS", "cores": cpu_cores(),
+            "kind": "oracle", "sample": f"fp64 oracle forward of the whole {w.name.split(':')[0]} "
+                                        f"workload, {runs} runs, {dt:.1f} s"}
 
 
 def kernel_source_sha(kernel_file):
