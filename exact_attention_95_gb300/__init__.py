@@ -9,6 +9,10 @@ is missing, every call raises; there is no fallback implementation.
 Functions carry the C names:
 
 * ``attn_fwd(Q, K, V, scale, causal, out_dtype=None) -> (O, LSE)``
+* ``attn_fwd_split(Q, K, V, scale, causal, num_splits=0, ...) -> (O, LSE)``: query
+  and key lengths may differ (bottom-right causal alignment); the key range may
+  be split, with the partial results merged
+* ``attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)``
 * ``attn_bwd(Q, K, V, O, dO, LSE, scale, causal) -> (dQ, dK, dV)``
 * ``attn_bwd_workspace_size(B, Hq, Hkv, N, d)``
 * ``attn_last_device_status(stream=None)``, ``attn_status_string(code)``
@@ -34,9 +38,9 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5
 ATTN_BF16, ATTN_F32 = 0, 1
 
-EXPORTED = ("attn_fwd", "attn_bwd", "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_convert",
-            "attn_bwd_workspace_size", "attn_status_string", "attn_last_device_status",
-            "attn_selftest_wait_timeout")
+EXPORTED = ("attn_fwd", "attn_fwd_split", "attn_fwd_split_workspace_size", "attn_bwd",
+            "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_convert", "attn_bwd_workspace_size",
+            "attn_status_string", "attn_last_device_status", "attn_selftest_wait_timeout")
 _BWD_STAGES = {"all": "attn_bwd", "preprocess": "attn_bwd_preprocess", "main": "attn_bwd_main",
                "convert": "attn_bwd_convert"}
 
@@ -69,6 +73,11 @@ def load_library(path: str = LIB_PATH):
             fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32,
                            i32, i32, vp, sz, vp]
             fn.restype = i32
+        lib.attn_fwd_split.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, i32,
+                                       vp, sz, vp]
+        lib.attn_fwd_split.restype = i32
+        lib.attn_fwd_split_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_fwd_split_workspace_size.restype = sz
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i32]
@@ -144,6 +153,47 @@ def attn_fwd(Q, K, V, scale=None, causal=False, out_dtype=None, O=None, LSE=None
                       float(scale), int(bool(causal)), in_dt, out_dt, _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
+    return O, LSE
+
+
+def attn_fwd_split_workspace_size(B: int, Hq: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
+    return int(load_library().attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits))
+
+
+def attn_fwd_split(Q, K, V, scale=None, causal=False, num_splits=0, out_dtype=None, O=None, LSE=None,
+                   workspace=None, stream=None):
+    """O, LSE of attention with Nq = Q.shape[2] queries and Nk = K.shape[2] keys
+    (bottom-right causal alignment when they differ), the key range cut into
+    num_splits parts (0: chosen by the library) whose partial results are
+    merged.  bf16 inputs; O bf16 (default) or fp32."""
+    lib = load_library()
+    B, Hq, Nq, d = Q.shape
+    Hkv, Nk = K.shape[1], K.shape[2]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bf = torch.bfloat16
+    if out_dtype is None:
+        out_dtype = bf
+    out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
+    _check_tensor("Q", Q, bf, (B, Hq, Nq, d))
+    _check_tensor("K", K, bf, (B, Hkv, Nk, d))
+    _check_tensor("V", V, bf, (B, Hkv, Nk, d))
+    if O is None:
+        O = torch.empty((B, Hq, Nq, d), dtype=out_dtype, device=Q.device)
+    if LSE is None:
+        LSE = torch.empty((B, Hq, Nq), dtype=torch.float32, device=Q.device)
+    _check_tensor("O", O, out_dtype, (B, Hq, Nq, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, Nq))
+    ws_bytes = attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)
+    if workspace is None and ws_bytes > 0:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=Q.device)
+    wptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
+    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    rc = lib.attn_fwd_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, Nq, Nk, d,
+                            float(scale), int(bool(causal)), out_dt, int(num_splits), wptr, wbytes,
+                            _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_split")
     return O, LSE
 
 

@@ -1,5 +1,6 @@
 // api.cu -- the C ABI declared in include/attn.h: argument checks, TMA
 // tensor-map construction, kernel launches and the device status word.
+#include <algorithm>
 #include <cmath>
 #include <cstdint>
 #include <mutex>
@@ -128,6 +129,81 @@ __global__ void selftest_wait_kernel(int* status, unsigned long long limit_ns) {
 }  // namespace
 }  // namespace attn
 
+namespace attn {
+namespace {
+
+constexpr int kMaxSplits = 256;
+
+// Number of key splits: the caller's, or (num_splits == 0) enough to give the
+// forward about two CTAs per SM, at most one split per 128-key tile.  The
+// result never leaves a split without a tile.  -1 for an invalid request.
+int fwd_splits(int B, int Hq, int Nq, int Nk, int num_splits) {
+  if (num_splits < 0 || num_splits > kMaxSplits) return -1;
+  const int ktiles = (Nk + 127) / 128;
+  int want = num_splits;
+  if (want == 0) {
+    int dev = 0, sms = 148;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    const long long ctas = (long long)B * Hq * (((Nq + 127) / 128 + 1) / 2);
+    want = (int)std::min<long long>(64, std::max<long long>(1, (2LL * sms + ctas - 1) / ctas));
+  }
+  want = std::min(want, ktiles);
+  const int per = (ktiles + want - 1) / want;
+  return (ktiles + per - 1) / per;
+}
+
+size_t fwd_split_lse_offset(long long rows, int d, int splits) {
+  return ((size_t)splits * rows * d * 4 + 255) / 256 * 256;
+}
+
+size_t fwd_split_workspace_bytes(int B, int Hq, int Nq, int d, int splits) {
+  const long long rows = (long long)B * Hq * Nq;
+  return fwd_split_lse_offset(rows, d, splits) + ((size_t)splits * rows * 4 + 255) / 256 * 256;
+}
+
+// The tcgen05 forward over key splits: splits == 1 writes O (bf16 or fp32)
+// and LSE; otherwise O and LSE are the fp32 partial arrays with the given
+// strides between splits.
+attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
+                         int Hkv, int Nq, int Nk, int d, float sl2, int causal, int out_f32, int splits,
+                         long long o_stride, long long lse_stride, cudaStream_t s) {
+  int* status = status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  CUtensorMap tq, tk, tv;
+  if (!make_map(&tq, Q, (long long)B * Hq, Nq, d, 128) || !make_map(&tk, K, (long long)B * Hkv, Nk, d, 128) ||
+      !make_map(&tv, V, (long long)B * Hkv, Nk, d, 128))
+    return ATTN_ERR_CUDA;
+  FwdParams p{};
+  p.O = O;
+  p.LSE = LSE;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = Nq;
+  p.Nk = Nk;
+  p.kv_off = causal ? Nk - Nq : 0;
+  const int ktiles = (Nk + 127) / 128;
+  p.n_splits = splits;
+  p.tiles_per_split = (ktiles + splits - 1) / splits;
+  p.o_split_stride = o_stride;
+  p.lse_split_stride = lse_stride;
+  p.n_qtiles = (Nq + 127) / 128;
+  p.n_pairs = (p.n_qtiles + 1) / 2;
+  p.head_group = head_group_for((size_t)Nk * d * 2 * 2, (long long)B * Hq, size_t(64) << 20);
+  if ((long long)B * Hq * p.n_pairs * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  p.scale_log2 = sl2;
+  p.causal = causal;
+  p.out_f32 = out_f32;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e = launch_fwd_bf16(d, tq, tk, tv, p, s);
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+}  // namespace
+}  // namespace attn
+
 using namespace attn;
 
 extern "C" {
@@ -164,30 +240,43 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                                    Hkv, N, sl2, causal, s);
     return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
   }
-  int* status = status_ptr();
-  if (!status) return ATTN_ERR_CUDA;
-  CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, Q, (long long)B * Hq, N, d, 128) || !make_map(&tk, K, (long long)B * Hkv, N, d, 128) ||
-      !make_map(&tv, V, (long long)B * Hkv, N, d, 128))
-    return ATTN_ERR_CUDA;
-  FwdParams p{};
-  p.O = O;
-  p.LSE = LSE;
-  p.status = status;
-  p.B = B;
-  p.Hq = Hq;
-  p.Hkv = Hkv;
-  p.N = N;
-  p.n_qtiles = (N + 127) / 128;
-  p.n_pairs = (p.n_qtiles + 1) / 2;
-  p.head_group = head_group_for((size_t)N * d * 2 * 2, (long long)B * Hq, size_t(64) << 20);
-  if ((long long)B * Hq * p.n_pairs > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
-  p.scale_log2 = sl2;
-  p.causal = causal;
-  p.out_f32 = out_dtype == ATTN_F32 ? 1 : 0;
-  p.wait_limit_ns = wait_limit();
-  cudaError_t e = launch_fwd_bf16(d, tq, tk, tv, p, s);
+  return fwd_bf16_run(Q, K, V, O, LSE, B, Hq, Hkv, N, N, d, sl2, causal, out_dtype == ATTN_F32, 1, 0, 0, s);
+}
+
+attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                           attn_dtype out_dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+  if (!Q || !K || !V || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_BF16 && out_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_shape(B, Hq, Hkv, Nq, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (Nk < 1) return ATTN_ERR_INVALID_ARG;
+  if ((Nk + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
+  const int splits = fwd_splits(B, Hq, Nq, Nk, num_splits);
+  if (splits < 1) return ATTN_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const float sl2 = scale * 1.4426950408889634f;
+  if (splits == 1)
+    return fwd_bf16_run(Q, K, V, O, LSE, B, Hq, Hkv, Nq, Nk, d, sl2, causal, out_dtype == ATTN_F32, 1, 0, 0, s);
+  const size_t need = fwd_split_workspace_bytes(B, Hq, Nq, d, splits);
+  if (!workspace || !aligned(workspace, 256) || workspace_bytes < need) return ATTN_ERR_INVALID_ARG;
+  const long long rows = (long long)B * Hq * Nq;
+  float* Opart = static_cast<float*>(workspace);
+  float* Lpart = reinterpret_cast<float*>(static_cast<char*>(workspace) + fwd_split_lse_offset(rows, d, splits));
+  st = fwd_bf16_run(Q, K, V, Opart, Lpart, B, Hq, Hkv, Nq, Nk, d, sl2, causal, 1, splits, rows * d, rows, s);
+  if (st != ATTN_OK) return st;
+  cudaError_t e = launch_fwd_merge(d, Opart, Lpart, O, LSE, rows, splits, out_dtype == ATTN_F32 ? 1 : 0, s);
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+size_t attn_fwd_split_workspace_size(int B, int Hq, int Nq, int Nk, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+  const int splits = fwd_splits(B, Hq, Nq, Nk, num_splits);
+  if (splits < 1) return 0;
+  return splits == 1 ? 0 : fwd_split_workspace_bytes(B, Hq, Nq, d, splits);
 }
 
 size_t attn_bwd_workspace_size(int B, int Hq, int Hkv, int N, int d) {

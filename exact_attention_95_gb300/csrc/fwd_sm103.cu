@@ -100,14 +100,26 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int lane = threadIdx.x & 31;
   // CTA -> (b*Hq + h, pair of query tiles), heaviest pairs first within groups of heads.
   int bh, rank;
-  grouped_order(blockIdx.x, p.B * p.Hq, p.n_pairs, p.head_group, bh, rank);
+  const int split = blockIdx.x % p.n_splits;
+  grouped_order(blockIdx.x / p.n_splits, p.B * p.Hq, p.n_pairs, p.head_group, bh, rank);
   const int pair = p.n_pairs - 1 - rank;
   const int q0 = pair * 2 * kBM;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
   const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
-  int n_kv = (p.N + kBN - 1) / kBN;
-  if (p.causal) n_kv = min(n_kv, 2 * pair + 2);  // K/V tiles right of the diagonal are skipped
+  // K/V tiles [kt0, kt0 + n_kv): this CTA's split of the key range, without
+  // the tiles right of the causal diagonal of its last query row (never
+  // loaded).  An empty range writes O = 0 and LSE = -inf.
+  const int kt0 = split * p.tiles_per_split;
+  int kt_end = min(kt0 + p.tiles_per_split, (p.Nk + kBN - 1) / kBN);
+  if (p.causal) {
+    const int k_last = min(q0 + 2 * kBM, p.N) - 1 + p.kv_off;  // last key of the last row
+    kt_end = k_last < 0 ? 0 : min(kt_end, k_last / kBN + 1);
+  }
+  const int n_kv = max(0, kt_end - kt0);
+  float* const o_out = p.out_f32 ? static_cast<float*>(p.O) + split * p.o_split_stride : nullptr;
+  uint16_t* const o_out16 = p.out_f32 ? nullptr : static_cast<uint16_t*>(p.O);
+  float* const lse_out = p.LSE + split * p.lse_split_stride;
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_QFULL), 1);
@@ -137,7 +149,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp < 4) {
     regs_dec<kRegsLow>();
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && n_kv > 0) {
       // ---------------------------------------------------------- producer
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
@@ -177,13 +189,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* m = v ? &tmV : &tmK;
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
-                      j * kBN, bh_kv);
+                      (kt0 + j) * kBN, bh_kv);
       }
       // Drain: every issued copy must land before the CTA may exit.
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    } else if (warp == 1) {
+    } else if (warp == 1 && n_kv > 0) {
       // ---------------------------------------------------------- MMA issuer
       // The whole warp runs this loop (uniform operands); one elected lane issues.
       // Ring slots of the loads (see the producer): K_0 first, then K_{j+1}
@@ -278,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     float corr = 0.f;     // sum over tiles of (largest P - its bf16 rounding), same scale as l
     bool ok = true;
     for (int j = 0; j < n_kv; ++j) {
-      const int k0 = j * kBN;
+      const int k0 = (kt0 + j) * kBN;
       if (!mbar_wait(bar(C::B_SFULL + t), j & 1, wc)) {
         ok = false;
         break;
@@ -296,8 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_SFREE));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
-      if ((k0 + kBN > p.N) || (p.causal && k0 + kBN - 1 > qt0)) {
-        const int lim = p.causal ? min(p.N - 1, q) : p.N - 1;
+      if ((k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qt0 + p.kv_off)) {
+        const int lim = p.causal ? min(p.Nk - 1, q + p.kv_off) : p.Nk - 1;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -384,9 +396,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
     }
-    // Epilogue: O / l and LSE.
-    if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
-      tc_fence_after();
+    // Epilogue: O / l and LSE (O = 0, LSE = -inf when no key was in range).
+    const bool have = n_kv > 0;
+    if (ok && (!have || mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc))) {
+      if (have) tc_fence_after();
       // O is divided by the row sum less the rounding of each tile's largest
       // P: when one key dominates a row, its bf16 rounding then cancels
       // between O and the divisor.  LSE uses the exact sum.
@@ -397,18 +410,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
-        tmem_ld32(o_t + c * 32, o);
-        tmem_ld_wait(o);
+        if (have) {
+          tmem_ld32(o_t + c * 32, o);
+          tmem_ld_wait(o);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] = 0u;
+        }
         if (valid) {
           if (p.out_f32) {
-            float4* dst = reinterpret_cast<float4*>(static_cast<float*>(p.O) + row_idx * D + c * 32);
+            float4* dst = reinterpret_cast<float4*>(o_out + row_idx * D + c * 32);
 #pragma unroll
             for (int i = 0; i < 8; ++i)
               dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                    __uint_as_float(o[4 * i + 2]) * inv_l,
                                    __uint_as_float(o[4 * i + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) + row_idx * D + c * 32);
+            uint4* dst = reinterpret_cast<uint4*>(o_out16 + row_idx * D + c * 32);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               uint4 v;
@@ -423,7 +441,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       if (valid) {
         // LSE = ln(sum_j e^{s_j}) = (m + log2 l) * ln 2, m in log2 units.
-        p.LSE[row_idx] = (l > 0.f) ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+        lse_out[row_idx] = (l > 0.f) ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
       }
     }
   }
@@ -454,7 +472,7 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
   if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.Hq * p.n_pairs);
+  dim3 grid(p.B * p.Hq * p.n_pairs * p.n_splits);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }

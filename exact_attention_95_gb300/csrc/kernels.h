@@ -12,7 +12,13 @@ struct FwdParams {
   void* O;          // [B, Hq, N, d] bf16 or fp32
   float* LSE;       // [B, Hq, N] natural-log units
   int* status;      // device status word
-  int B, Hq, Hkv, N;
+  int B, Hq, Hkv, N;  // N: query rows per head
+  int Nk;           // keys per head (N for the plain forward)
+  int kv_off;       // causal: key j is kept for query i when j <= i + kv_off (Nk - N)
+  int n_splits;     // key range cut into n_splits parts of tiles_per_split 128-key tiles
+  int tiles_per_split;
+  long long o_split_stride;    // elements between the O outputs of consecutive splits
+  long long lse_split_stride;  // same for LSE
   int n_qtiles;     // ceil(N / 128)
   int n_pairs;      // ceil(n_qtiles / 2): each CTA owns two 128-row query tiles
   int head_group;   // heads whose CTAs are launched together (L2 reuse of K/V)
@@ -27,6 +33,12 @@ struct FwdParams {
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
 size_t fwd_bf16_smem_bytes(int d);
+
+// Merge of a split forward's partial results: Opart [n_splits][rows][d] fp32
+// (each normalised over its part), Lpart [n_splits][rows] fp32 (natural log)
+// -> O [rows][d] (bf16 or fp32) and LSE [rows].
+cudaError_t launch_fwd_merge(int d, const float* Opart, const float* Lpart, void* O, float* LSE, long long rows,
+                             int n_splits, int out_f32, cudaStream_t stream);
 
 // fp32 SIMT forward (exact fp32 arithmetic, FFMA + ex2).
 cudaError_t launch_fwd_f32(int d, const float* Q, const float* K, const float* V, float* O,

@@ -77,6 +77,39 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
                      attn_dtype in_dtype, attn_dtype out_dtype, void* stream);
 
 /*
+ * Forward with separate query and key lengths and an optional split of the
+ * key range.  With Nq != Nk the causal mask is aligned to the bottom-right
+ * corner ("从Online-Softmax…" 0x09): key j is kept for query i when
+ * j <= i + (Nk - Nq); a query row with no kept key gets O = 0 and LSE = -inf.
+ * The key range can be cut into num_splits contiguous parts (whole 128-key
+ * tiles) that run in parallel and write partial (O, LSE) pairs, which a
+ * merge kernel combines with the online-softmax merge ("02 FlashAttention"
+ * §5; §12.1 applies it to key splits, FlashDecoding): LSE = ln sum_s e^{LSE_s},
+ * O = sum_s e^{LSE_s - LSE} O_s.  This fills the GPU when B * Hq * ceil(Nq/256)
+ * is small (decoding: Nq = 1 or a few rows against a long key range).
+ *
+ *   Q [B,Hq,Nq,d], K and V [B,Hkv,Nk,d]  bf16
+ *   O [B,Hq,Nq,d]                        out_dtype: bf16 or fp32
+ *   LSE [B,Hq,Nq] fp32
+ *   B, Hq, Hkv, Nq, Nk >= 1; Hq % Hkv == 0; d in {64, 128}; causal in {0, 1}.
+ *   num_splits: 0 chooses (about two CTAs per SM), else 1..256; it is capped
+ *     at one split per 128-key tile and rounded so that no split is empty.
+ *   workspace: attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)
+ *     bytes, 256-byte aligned, owned by the caller, not shared with a
+ *     concurrent call; NULL is allowed when that size is 0 (one split).
+ * O and LSE are fully overwritten.  Inputs are not modified.  Errors as for
+ * attn_fwd (a missing or short workspace: ATTN_ERR_INVALID_ARG).
+ */
+attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                           int B, int Hq, int Hkv, int Nq, int Nk, int d, float scale, int causal,
+                           attn_dtype out_dtype, int num_splits, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Bytes of workspace attn_fwd_split needs for these sizes and num_splits
+ * (0 when the key range is not split); 0 on bad sizes. */
+size_t attn_fwd_split_workspace_size(int B, int Hq, int Nq, int Nk, int d, int num_splits);
+
+/*
  * Backward of O with respect to Q, K, V given dO (no gradient through LSE).
  * The probabilities are recomputed per tile from the saved LSE
  * ("从Online-Softmax…" 0x04: recompute instead of storing S and P;

@@ -108,3 +108,48 @@ def test_missing_library_fails_loudly(tmp_path):
             mod.load_library(str(tmp_path / "missing.so"))
         finally:
             mod._lib = saved
+
+
+def _split_ws(rows, d, splits):
+    o = (splits * rows * d * 4 + 255) // 256 * 256
+    return o + (splits * rows * 4 + 255) // 256 * 256
+
+
+def test_fwd_split_workspace_size(lib):
+    ws = pkg.attn_fwd_split_workspace_size
+    assert ws(1, 4, 1, 4096, 128, 1) == 0  # one split: written directly, no workspace
+    # 8 key tiles in 4 splits of 2.
+    assert ws(2, 4, 3, 1024, 128, 4) == _split_ws(2 * 4 * 3, 128, 4)
+    # More splits than tiles are capped at one split per tile.
+    assert ws(1, 2, 5, 200, 64, 5) == _split_ws(1 * 2 * 5, 64, 2)
+    # 8 tiles over 7 requested splits: tiles of 2, hence 4 non-empty splits.
+    assert ws(1, 1, 1, 1024, 64, 7) == _split_ws(1, 64, 4)
+    assert ws(1, 1, 1, 1024, 64, -1) == 0
+    assert ws(1, 1, 1, 1024, 64, 257) == 0
+    assert ws(1, 1, 0, 1024, 64, 2) == 0
+    assert ws(1, 1, 1, 1024, 96, 2) == 0
+
+
+def _fwd_split(lib, **kw):
+    a = dict(Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, Nq=16, Nk=1024, d=64, scale=0.125, causal=1,
+             outd=0, splits=4, ws=None, wsb=0)
+    a.update(kw)
+    return lib.attn_fwd_split(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["Hq"], a["Hkv"],
+                              a["Nq"], a["Nk"], a["d"], a["scale"], a["causal"], a["outd"], a["splits"],
+                              a["ws"], a["wsb"], None)
+
+
+def test_fwd_split_argument_errors(lib):
+    assert _fwd_split(lib, Q=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, Nk=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, Nq=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, splits=-2) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, splits=300) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, outd=7) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, d=256) == pkg.ATTN_ERR_UNSUPPORTED
+    assert _fwd_split(lib, Hq=3, Hkv=2) == pkg.ATTN_ERR_INVALID_ARG
+    # A split run needs the workspace: missing, short or misaligned.
+    assert _fwd_split(lib) == pkg.ATTN_ERR_INVALID_ARG
+    need = pkg.attn_fwd_split_workspace_size(1, 2, 16, 1024, 64, 4)
+    assert _fwd_split(lib, ws=A, wsb=need - 1) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd_split(lib, ws=ctypes.c_void_p(0x10010), wsb=need) == pkg.ATTN_ERR_INVALID_ARG
