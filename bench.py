@@ -268,6 +268,8 @@ def run_native(args):
     from exact_attention_95_gb300 import inputs
 
     pkg.load_library()
+    if args.workload == "decode":
+        return run_decode(args, pkg, rank, world, dev)
     w = inputs.WORKLOADS[args.workload]
     if w.dtype != "bf16" or not w.backward:
         return run_fwd_only(args, w, pkg, rank, world, dev)
@@ -496,6 +498,102 @@ def run_fwd_only(args, w, pkg, rank, world, dev):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline_fwd(w, args.cpu_budget)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+# Decode shape of the split-key forward: one query row per head against a long
+# key range (GQA, causal; bottom-right alignment keeps every key for the row).
+DECODE = dict(B=1, Hq=32, Hkv=8, Nq=1, Nk=131072, d=128, causal=True)
+
+
+def run_decode(args, pkg, rank, world, dev):
+    """attn_fwd_split on the decode shape: HBM-bound (K and V are read once),
+    so the roofline is bytes per second against the measured copy rate.  The
+    same call with one split (no key split) is timed alongside."""
+    import numpy as np
+    import torch
+    from exact_attention_95_gb300 import inputs
+
+    c = DECODE
+    seed = 0x5EED0000 + 16 * 9
+    Q = torch.from_numpy(inputs.make_tensor(seed, (c["B"], c["Hq"], c["Nq"], c["d"]), "bf16").view(np.int16))
+    K = torch.from_numpy(inputs.make_tensor(seed + 1, (c["B"], c["Hkv"], c["Nk"], c["d"]), "bf16").view(np.int16))
+    V = torch.from_numpy(inputs.make_tensor(seed + 2, (c["B"], c["Hkv"], c["Nk"], c["d"]), "bf16").view(np.int16))
+    Q, K, V = (t.view(torch.bfloat16).to(dev) for t in (Q, K, V))
+    stream = torch.cuda.current_stream()
+    scale = 1.0 / math.sqrt(c["d"])
+
+    def timed(splits, steps):
+        ws_n = pkg.attn_fwd_split_workspace_size(c["B"], c["Hq"], c["Nq"], c["Nk"], c["d"], splits)
+        ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
+        O = torch.empty(c["B"], c["Hq"], c["Nq"], c["d"], dtype=torch.bfloat16, device=dev)
+        L = torch.empty(c["B"], c["Hq"], c["Nq"], dtype=torch.float32, device=dev)
+        run = lambda: pkg.attn_fwd_split(Q, K, V, scale, c["causal"], num_splits=splits, O=O, LSE=L,
+                                         workspace=ws, stream=stream)
+        for _ in range(max(3, args.warmup)):
+            run()
+        torch.cuda.synchronize()
+        if pkg.attn_last_device_status() != pkg.ATTN_OK:
+            raise RuntimeError("device status not OK")
+        flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+        for e0, e1 in evs:
+            flush.zero_()  # K and V (537 MB) exceed L2 anyway; this keeps the steps alike
+            e0.record(stream)
+            run()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs)
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(dev.index)
+    barrier()
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        ms = timed(0, args.steps)
+        wall = time.perf_counter() - wall0
+    ms_one = timed(1, max(3, args.steps // 4))
+    ms = max_over_ranks(ms, dev)
+    flops = 4.0 * c["Nq"] * c["Nk"] * c["d"] * c["Hq"] * c["B"]
+    kv_bytes = 2.0 * c["B"] * c["Hkv"] * c["Nk"] * c["d"] * 2
+    io_bytes = kv_bytes + 2.0 * c["B"] * c["Hq"] * c["Nq"] * c["d"] * 2 + 4.0 * c["B"] * c["Hq"] * c["Nq"]
+    peaks, peak_src = load_peaks()
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAK["hbm_gbs"]))
+    gbs = io_bytes / (ms / 1e3) / 1e9
+    # e2e through the public API: Q, K, V from pinned host memory, O back.
+    hQ, hK, hV = (t.cpu().pin_memory() for t in (Q, K, V))
+    hO = torch.empty(c["B"], c["Hq"], c["Nq"], c["d"], dtype=torch.bfloat16).pin_memory()
+    e_steps = max(1, min(args.e2e_steps, 5))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e_steps):
+        dq, dk, dv = (t.to(dev, non_blocking=True) for t in (hQ, hK, hV))
+        o, _ = pkg.attn_fwd_split(dq, dk, dv, scale, c["causal"], num_splits=0, stream=stream)
+        hO.copy_(o, non_blocking=True)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e_ms = e0.elapsed_time(e1) / e_steps
+    line = {
+        "metric": METRIC, "value": flops * world / (ms / 1e3) / 1e12, "unit": "TFLOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1), bf16)",
+        "config": {"workload": "decode: attn_fwd_split, B1 Hq32 Hkv8 Nq1 Nk131072 d128 causal, library-chosen splits",
+                   **c, "l2": "K and V (537 MB) exceed the 126 MiB L2; 256 MiB written between steps",
+                   "parallelism": f"replicas x{world} (weak)"},
+        "fwd": {"ms": ms, "ms_one_split": ms_one, "speedup_vs_one_split": ms_one / ms},
+        "roofline": {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+                     "traffic": None, "kernel": "fwd_bf16_kernel + fwd_merge_kernel (attn_fwd_split)",
+                     "peak_source": f"hbm_gbs of {peak_src}"},
+        "e2e": {"value": flops * world / (e_ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": e_ms,
+                "h2d_bytes_per_step": sum(t.numel() * 2 for t in (hQ, hK, hV)),
+                "d2h_bytes_per_step": hO.numel() * 2},
+        "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
     if rank == 0:
         print(json.dumps(line), flush=True)
     return 0

@@ -81,7 +81,10 @@ struct Fwd {
   static constexpr uint32_t TM_O = 256;  // + D * t
 };
 
-template <int D>
+// ONE: every CTA computes query tile 0 only (N <= 128: decoding and short
+// sequences), with its own MMA schedule; otherwise both tiles (a last pair
+// whose second tile has no row below N still computes it, on zero rows).
+template <int D, bool ONE>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -117,6 +120,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     kt_end = k_last < 0 ? 0 : min(kt_end, k_last / kBN + 1);
   }
   const int n_kv = max(0, kt_end - kt0);
+  constexpr bool two = !ONE;
   float* const o_out = p.out_f32 ? static_cast<float*>(p.O) + split * p.o_split_stride : nullptr;
   uint16_t* const o_out16 = p.out_f32 ? nullptr : static_cast<uint16_t*>(p.O);
   float* const lse_out = p.LSE + split * p.lse_split_stride;
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         tc_commit_warp(bar(C::B_SFULL + t));
-        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // K_j read by both tiles
+        if (t == 1 || !two) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // K_j read by every tile
       };
       // O_t += P_t V_j (A = 16 keys of P_t = 8 TMEM columns; B = 16 V rows, MN-major).
       auto issue_pv = [&](int t, int j) {
@@ -231,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
                       (kk > 0 || j > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_ODONE + t));
-        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // V_j read by both tiles
+        if (t == 1 || !two) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // V_j read by every tile
       };
       // The S buffer passes between the tiles: S_0(j), S_1(j), S_0(j+1), ...
       // Each S is issued once the previous one has been read out (SFREE).
@@ -242,6 +246,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         return r;
       };
       if (ok) ok = wait_kv(k_li(0));
+      if (ok && !two) {
+        // Tile 0 alone: S_0(j+1) as soon as S_0(j) has been read (P_0 has its
+        // own columns), then P_0 V_j.
+        issue_s(0, 0);
+        for (int j = 0; j < n_kv && ok; ++j) {
+          if (j + 1 < n_kv) {
+            if (!wait_sfree() || !wait_kv(k_li(j + 1))) break;
+            issue_s(0, j + 1);
+          }
+          if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + 0), j & 1, wc)) break;
+          tc_fence_after();
+          issue_pv(0, j);
+        }
+        ok = false;  // the two-tile schedule below does not run
+      }
       if (ok) {
         issue_s(0, 0);
         ok = wait_sfree();
@@ -289,7 +308,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     float l = 0.f;        // running sum of 2^(scale*s*log2e - m): gives LSE
     float corr = 0.f;     // sum over tiles of (largest P - its bf16 rounding), same scale as l
     bool ok = true;
-    for (int j = 0; j < n_kv; ++j) {
+    const bool active = t == 0 || two;  // tile 1 of a one-tile CTA has no rows
+    for (int j = 0; j < (active ? n_kv : 0); ++j) {
       const int k0 = (kt0 + j) * kBN;
       if (!mbar_wait(bar(C::B_SFULL + t), j & 1, wc)) {
         ok = false;
@@ -398,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Epilogue: O / l and LSE (O = 0, LSE = -inf when no key was in range).
     const bool have = n_kv > 0;
-    if (ok && (!have || mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc))) {
+    if (ok && active && (!have || mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc))) {
       if (have) tc_fence_after();
       // O is divided by the row sum less the rounding of each tile's largest
       // P: when one key dominates a row, its bf16 rounding then cancels
@@ -454,15 +474,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
-                   const FwdParams& p, cudaStream_t stream) {
+template <int D, bool ONE>
+cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                       const FwdParams& p, cudaStream_t stream) {
   using C = Fwd<D>;
-  auto kern = fwd_bf16_kernel<D>;
+  auto kern = fwd_bf16_kernel<D, ONE>;
   // setmaxnreg moves registers inside the launch allocation; refuse to launch
   // if the compiler gave the kernel a different per-thread count than assumed
   // (a larger split than the allocation would leave setmaxnreg.inc waiting).
-  static int regs = -1;
+  static int regs = -1;  // one per instantiation
   if (regs < 0) {
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -485,8 +505,11 @@ size_t fwd_bf16_smem_bytes(int d) {
 
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {
-  if (d == 128) return launch<128>(tmQ, tmK, tmV, p, stream);
-  if (d == 64) return launch<64>(tmQ, tmK, tmV, p, stream);
+  const bool one = p.N <= kBM;
+  if (d == 128) return one ? launch_one<128, true>(tmQ, tmK, tmV, p, stream)
+                           : launch_one<128, false>(tmQ, tmK, tmV, p, stream);
+  if (d == 64) return one ? launch_one<64, true>(tmQ, tmK, tmV, p, stream)
+                          : launch_one<64, false>(tmQ, tmK, tmV, p, stream);
   return cudaErrorInvalidValue;
 }
 
