@@ -526,7 +526,7 @@ def run_decode(args, pkg, rank, world, dev):
     scale = 1.0 / math.sqrt(c["d"])
 
     def timed(splits, steps):
-        ws_n = pkg.attn_fwd_split_workspace_size(c["B"], c["Hq"], c["Nq"], c["Nk"], c["d"], splits)
+        ws_n = pkg.attn_fwd_split_workspace_size(c["B"], c["Hq"], c["Hkv"], c["Nq"], c["Nk"], c["d"], splits)
         ws = torch.empty(max(ws_n, 1), dtype=torch.uint8, device=dev)
         O = torch.empty(c["B"], c["Hq"], c["Nq"], c["d"], dtype=torch.bfloat16, device=dev)
         L = torch.empty(c["B"], c["Hq"], c["Nq"], dtype=torch.float32, device=dev)

@@ -12,7 +12,7 @@ Functions carry the C names:
 * ``attn_fwd_split(Q, K, V, scale, causal, num_splits=0, ...) -> (O, LSE)``: query
   and key lengths may differ (bottom-right causal alignment); the key range may
   be split, with the partial results merged
-* ``attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)``
+* ``attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)``
 * ``attn_bwd(Q, K, V, O, dO, LSE, scale, causal) -> (dQ, dK, dV)``
 * ``attn_bwd_workspace_size(B, Hq, Hkv, N, d)``
 * ``attn_last_device_status(stream=None)``, ``attn_status_string(code)``
@@ -76,7 +76,7 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_split.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, i32, i32, i32,
                                        vp, sz, vp]
         lib.attn_fwd_split.restype = i32
-        lib.attn_fwd_split_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32]
+        lib.attn_fwd_split_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.attn_fwd_split_workspace_size.restype = sz
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = sz
@@ -156,8 +156,9 @@ def attn_fwd(Q, K, V, scale=None, causal=False, out_dtype=None, O=None, LSE=None
     return O, LSE
 
 
-def attn_fwd_split_workspace_size(B: int, Hq: int, Nq: int, Nk: int, d: int, num_splits: int = 0) -> int:
-    return int(load_library().attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits))
+def attn_fwd_split_workspace_size(B: int, Hq: int, Hkv: int, Nq: int, Nk: int, d: int,
+                                  num_splits: int = 0) -> int:
+    return int(load_library().attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits))
 
 
 def attn_fwd_split(Q, K, V, scale=None, causal=False, num_splits=0, out_dtype=None, O=None, LSE=None,
@@ -184,7 +185,7 @@ def attn_fwd_split(Q, K, V, scale=None, causal=False, num_splits=0, out_dtype=No
         LSE = torch.empty((B, Hq, Nq), dtype=torch.float32, device=Q.device)
     _check_tensor("O", O, out_dtype, (B, Hq, Nq, d))
     _check_tensor("LSE", LSE, torch.float32, (B, Hq, Nq))
-    ws_bytes = attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)
+    ws_bytes = attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)
     if workspace is None and ws_bytes > 0:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=Q.device)
     wptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)

@@ -137,7 +137,7 @@ constexpr int kMaxSplits = 256;
 // Number of key splits: the caller's, or (num_splits == 0) enough to give the
 // forward about two CTAs per SM, at most one split per 128-key tile.  The
 // result never leaves a split without a tile.  -1 for an invalid request.
-int fwd_splits(int B, int Hq, int Nq, int Nk, int num_splits) {
+int fwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits) {
   if (num_splits < 0 || num_splits > kMaxSplits) return -1;
   const int ktiles = (Nk + 127) / 128;
   int want = num_splits;
@@ -145,7 +145,9 @@ int fwd_splits(int B, int Hq, int Nq, int Nk, int num_splits) {
     int dev = 0, sms = 148;
     cudaGetDevice(&dev);
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const long long ctas = (long long)B * Hq * (((Nq + 127) / 128 + 1) / 2);
+    const int G = Hq / Hkv;
+    const bool packed = G > 1 && (long long)G * Nq <= 128;  // as in fwd_bf16_run
+    const long long ctas = packed ? (long long)B * Hkv : (long long)B * Hq * (((Nq + 127) / 128 + 1) / 2);
     want = (int)std::min<long long>(64, std::max<long long>(1, (2LL * sms + ctas - 1) / ctas));
   }
   want = std::min(want, ktiles);
@@ -170,11 +172,19 @@ attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, f
                          long long o_stride, long long lse_stride, cudaStream_t s) {
   int* status = status_ptr();
   if (!status) return ATTN_ERR_CUDA;
+  // GQA packing when the whole group fits one 128-row tile (decoding).
+  const int G = Hq / Hkv;
+  const bool packed = G > 1 && (long long)G * Nq <= 128;
+  const long long heads = packed ? (long long)B * Hkv : (long long)B * Hq;
+  const int rows = packed ? G * Nq : Nq;
   CUtensorMap tq, tk, tv;
-  if (!make_map(&tq, Q, (long long)B * Hq, Nq, d, 128) || !make_map(&tk, K, (long long)B * Hkv, Nk, d, 128) ||
+  if (!make_map(&tq, Q, heads, rows, d, 128) || !make_map(&tk, K, (long long)B * Hkv, Nk, d, 128) ||
       !make_map(&tv, V, (long long)B * Hkv, Nk, d, 128))
     return ATTN_ERR_CUDA;
   FwdParams p{};
+  p.packed = packed ? 1 : 0;
+  p.heads = (int)heads;
+  p.rows = rows;
   p.O = O;
   p.LSE = LSE;
   p.status = status;
@@ -189,10 +199,10 @@ attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, f
   p.tiles_per_split = (ktiles + splits - 1) / splits;
   p.o_split_stride = o_stride;
   p.lse_split_stride = lse_stride;
-  p.n_qtiles = (Nq + 127) / 128;
+  p.n_qtiles = (rows + 127) / 128;
   p.n_pairs = (p.n_qtiles + 1) / 2;
-  p.head_group = head_group_for((size_t)Nk * d * 2 * 2, (long long)B * Hq, size_t(64) << 20);
-  if ((long long)B * Hq * p.n_pairs * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  p.head_group = head_group_for((size_t)Nk * d * 2 * 2, heads, size_t(64) << 20);
+  if (heads * p.n_pairs * splits > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
   p.scale_log2 = sl2;
   p.causal = causal;
   p.out_f32 = out_f32;
@@ -255,7 +265,7 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
   if (st != ATTN_OK) return st;
   if (Nk < 1) return ATTN_ERR_INVALID_ARG;
   if ((Nk + 127) / 128 > 65535) return ATTN_ERR_UNSUPPORTED;
-  const int splits = fwd_splits(B, Hq, Nq, Nk, num_splits);
+  const int splits = fwd_splits(B, Hq, Hkv, Nq, Nk, num_splits);
   if (splits < 1) return ATTN_ERR_INVALID_ARG;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const float sl2 = scale * 1.4426950408889634f;
@@ -272,9 +282,9 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
-size_t attn_fwd_split_workspace_size(int B, int Hq, int Nq, int Nk, int d, int num_splits) {
-  if (B < 1 || Hq < 1 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
-  const int splits = fwd_splits(B, Hq, Nq, Nk, num_splits);
+size_t attn_fwd_split_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {
+  if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
+  const int splits = fwd_splits(B, Hq, Hkv, Nq, Nk, num_splits);
   if (splits < 1) return 0;
   return splits == 1 ? 0 : fwd_split_workspace_bytes(B, Hq, Nq, d, splits);
 }

@@ -104,19 +104,20 @@ __global__ void __launch_bounds__(kThreads, 1)
   // CTA -> (b*Hq + h, pair of query tiles), heaviest pairs first within groups of heads.
   int bh, rank;
   const int split = blockIdx.x % p.n_splits;
-  grouped_order(blockIdx.x / p.n_splits, p.B * p.Hq, p.n_pairs, p.head_group, bh, rank);
+  grouped_order(blockIdx.x / p.n_splits, p.heads, p.n_pairs, p.head_group, bh, rank);
   const int pair = p.n_pairs - 1 - rank;
   const int q0 = pair * 2 * kBM;
   const int b = bh / p.Hq;
   const int h = bh - b * p.Hq;
-  const int bh_kv = b * p.Hkv + h / (p.Hq / p.Hkv);
+  const int bh_kv = p.packed ? bh : b * p.Hkv + h / (p.Hq / p.Hkv);
   // K/V tiles [kt0, kt0 + n_kv): this CTA's split of the key range, without
   // the tiles right of the causal diagonal of its last query row (never
   // loaded).  An empty range writes O = 0 and LSE = -inf.
   const int kt0 = split * p.tiles_per_split;
   int kt_end = min(kt0 + p.tiles_per_split, (p.Nk + kBN - 1) / kBN);
   if (p.causal) {
-    const int k_last = min(q0 + 2 * kBM, p.N) - 1 + p.kv_off;  // last key of the last row
+    // Last key of the tile's last query (of its largest query index when packed).
+    const int k_last = (p.packed ? p.N : min(q0 + 2 * kBM, p.N)) - 1 + p.kv_off;
     kt_end = k_last < 0 ? 0 : min(kt_end, k_last / kBN + 1);
   }
   const int n_kv = max(0, kt_end - kt0);
@@ -298,7 +299,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int quad = warp & 3;      // TMEM lane quarter this warp may access
     const int row = quad * 32 + lane;
     const int qt0 = q0 + t * kBM;
-    const int q = qt0 + row;
+    const int q = qt0 + row;                   // row of the grid head
+    const int qc = p.packed ? q % p.N : q;     // its query index (causal limit)
+    const int qc0 = p.packed ? 0 : qt0;        // smallest query index in the tile
     const uint32_t lane_off = (uint32_t)(quad * 32) << 16;
     const uint32_t s_t = tmem + lane_off + C::TM_S;  // shared S buffer
     const uint32_t p_t = tmem + lane_off + C::TM_P + t * 64;
@@ -328,8 +331,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_SFREE));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
-      if ((k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qt0 + p.kv_off)) {
-        const int lim = p.causal ? min(p.Nk - 1, q + p.kv_off) : p.Nk - 1;
+      if ((k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qc0 + p.kv_off)) {
+        const int lim = p.causal ? min(p.Nk - 1, qc + p.kv_off) : p.Nk - 1;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -425,8 +428,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       // between O and the divisor.  LSE uses the exact sum.
       const float lo = l - corr;
       const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
-      const bool valid = q < p.N;
-      const size_t row_idx = (size_t)bh * p.N + q;
+      const bool valid = q < p.rows;
+      const size_t row_idx = (size_t)bh * p.rows + q;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -492,7 +495,7 @@ cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUt
   if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
   if (e != cudaSuccess) return e;
-  dim3 grid(p.B * p.Hq * p.n_pairs * p.n_splits);
+  dim3 grid(p.heads * p.n_pairs * p.n_splits);
   kern<<<grid, kThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, p);
   return cudaGetLastError();
 }
@@ -505,7 +508,7 @@ size_t fwd_bf16_smem_bytes(int d) {
 
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {
-  const bool one = p.N <= kBM;
+  const bool one = p.rows <= kBM;
   if (d == 128) return one ? launch_one<128, true>(tmQ, tmK, tmV, p, stream)
                            : launch_one<128, false>(tmQ, tmK, tmV, p, stream);
   if (d == 64) return one ? launch_one<64, true>(tmQ, tmK, tmV, p, stream)

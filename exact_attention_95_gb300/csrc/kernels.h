@@ -19,7 +19,13 @@ struct FwdParams {
   int tiles_per_split;
   long long o_split_stride;    // elements between the O outputs of consecutive splits
   long long lse_split_stride;  // same for LSE
-  int n_qtiles;     // ceil(N / 128)
+  // GQA packing: with packed = 1 the G = Hq / Hkv query heads of a kv head
+  // share one tile, whose row r is query r % N of head r / N of the group
+  // (the heads of a group are adjacent, so their rows are contiguous).
+  int packed;
+  int heads;        // grid heads: B * Hq, or B * Hkv when packed
+  int rows;         // rows per grid head: N, or G * N when packed
+  int n_qtiles;     // ceil(rows / 128)
   int n_pairs;      // ceil(n_qtiles / 2): each CTA owns two 128-row query tiles
   int head_group;   // heads whose CTAs are launched together (L2 reuse of K/V)
   float scale_log2; // scale * log2(e)

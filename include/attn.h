@@ -86,7 +86,9 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
  * merge kernel combines with the online-softmax merge ("02 FlashAttention"
  * §5; §12.1 applies it to key splits, FlashDecoding): LSE = ln sum_s e^{LSE_s},
  * O = sum_s e^{LSE_s - LSE} O_s.  This fills the GPU when B * Hq * ceil(Nq/256)
- * is small (decoding: Nq = 1 or a few rows against a long key range).
+ * is small (decoding: Nq = 1 or a few rows against a long key range).  When
+ * the G = Hq / Hkv query heads of a kv head have G * Nq <= 128 rows in all,
+ * they share one 128-row tile (and one pass over K and V).
  *
  *   Q [B,Hq,Nq,d], K and V [B,Hkv,Nk,d]  bf16
  *   O [B,Hq,Nq,d]                        out_dtype: bf16 or fp32
@@ -94,7 +96,7 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
  *   B, Hq, Hkv, Nq, Nk >= 1; Hq % Hkv == 0; d in {64, 128}; causal in {0, 1}.
  *   num_splits: 0 chooses (about two CTAs per SM), else 1..256; it is capped
  *     at one split per 128-key tile and rounded so that no split is empty.
- *   workspace: attn_fwd_split_workspace_size(B, Hq, Nq, Nk, d, num_splits)
+ *   workspace: attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)
  *     bytes, 256-byte aligned, owned by the caller, not shared with a
  *     concurrent call; NULL is allowed when that size is 0 (one split).
  * O and LSE are fully overwritten.  Inputs are not modified.  Errors as for
@@ -107,7 +109,7 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
 
 /* Bytes of workspace attn_fwd_split needs for these sizes and num_splits
  * (0 when the key range is not split); 0 on bad sizes. */
-size_t attn_fwd_split_workspace_size(int B, int Hq, int Nq, int Nk, int d, int num_splits);
+size_t attn_fwd_split_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);
 
 /*
  * Backward of O with respect to Q, K, V given dO (no gradient through LSE).

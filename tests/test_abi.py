@@ -117,17 +117,18 @@ def _split_ws(rows, d, splits):
 
 def test_fwd_split_workspace_size(lib):
     ws = pkg.attn_fwd_split_workspace_size
-    assert ws(1, 4, 1, 4096, 128, 1) == 0  # one split: written directly, no workspace
+    assert ws(1, 4, 2, 1, 4096, 128, 1) == 0  # one split: written directly, no workspace
     # 8 key tiles in 4 splits of 2.
-    assert ws(2, 4, 3, 1024, 128, 4) == _split_ws(2 * 4 * 3, 128, 4)
+    assert ws(2, 4, 2, 3, 1024, 128, 4) == _split_ws(2 * 4 * 3, 128, 4)
     # More splits than tiles are capped at one split per tile.
-    assert ws(1, 2, 5, 200, 64, 5) == _split_ws(1 * 2 * 5, 64, 2)
+    assert ws(1, 2, 1, 5, 200, 64, 5) == _split_ws(1 * 2 * 5, 64, 2)
     # 8 tiles over 7 requested splits: tiles of 2, hence 4 non-empty splits.
-    assert ws(1, 1, 1, 1024, 64, 7) == _split_ws(1, 64, 4)
-    assert ws(1, 1, 1, 1024, 64, -1) == 0
-    assert ws(1, 1, 1, 1024, 64, 257) == 0
-    assert ws(1, 1, 0, 1024, 64, 2) == 0
-    assert ws(1, 1, 1, 1024, 96, 2) == 0
+    assert ws(1, 1, 1, 1, 1024, 64, 7) == _split_ws(1, 64, 4)
+    assert ws(1, 1, 1, 1, 1024, 64, -1) == 0
+    assert ws(1, 1, 1, 1, 1024, 64, 257) == 0
+    assert ws(1, 1, 1, 0, 1024, 64, 2) == 0
+    assert ws(1, 1, 1, 1, 1024, 96, 2) == 0
+    assert ws(1, 3, 2, 1, 1024, 64, 2) == 0  # Hq % Hkv
 
 
 def _fwd_split(lib, **kw):
@@ -150,6 +151,6 @@ def test_fwd_split_argument_errors(lib):
     assert _fwd_split(lib, Hq=3, Hkv=2) == pkg.ATTN_ERR_INVALID_ARG
     # A split run needs the workspace: missing, short or misaligned.
     assert _fwd_split(lib) == pkg.ATTN_ERR_INVALID_ARG
-    need = pkg.attn_fwd_split_workspace_size(1, 2, 16, 1024, 64, 4)
+    need = pkg.attn_fwd_split_workspace_size(1, 2, 1, 16, 1024, 64, 4)
     assert _fwd_split(lib, ws=A, wsb=need - 1) == pkg.ATTN_ERR_INVALID_ARG
     assert _fwd_split(lib, ws=ctypes.c_void_p(0x10010), wsb=need) == pkg.ATTN_ERR_INVALID_ARG

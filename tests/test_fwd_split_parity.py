@@ -55,6 +55,12 @@ CASES = [
     (1, 1, 1, 64, 200, 64, False, 4),    # more splits than tiles
     (1, 1, 1, 128, 1024, 128, False, 8),  # one tile per split
     (1, 8, 8, 256, 8192, 128, True, 0),
+    # GQA packing: the G query heads of a kv head share one tile when G * Nq <= 128.
+    (2, 8, 2, 16, 700, 64, True, 3),
+    (1, 16, 1, 8, 1000, 128, True, 0),    # exactly 128 packed rows
+    (1, 16, 1, 9, 1000, 128, True, 2),    # 144 rows: not packed
+    (1, 4, 1, 20, 10, 64, True, 1),       # packed, Nq > Nk: rows i < 10 keep no key
+    (1, 32, 8, 1, 131072, 128, True, 0),  # the decode benchmark shape
 ]
 
 
