@@ -61,6 +61,9 @@ def _load():
             lib.oracle_bwd.argtypes = [dp, dp, dp, dp] + shape + [dp, dp, dp, dp, dp, dp, i32]
             lib.oracle_bwd_dq_rows.argtypes = [dp, dp, dp, dp] + shape + [lp, i64, dp, i32]
             lib.oracle_bwd_dkv_rows.argtypes = [dp, dp, dp, dp, dp, dp] + shape + [lp, i64, dp, dp, i32]
+            u8p = ctypes.POINTER(ctypes.c_uint8)
+            lib.oracle_fwd_masked.argtypes = [dp, dp, dp] + shape + [u8p, i32, i64, dp, dp, i32]
+            lib.oracle_bwd_masked.argtypes = [dp, dp, dp, dp] + shape + [u8p, i32, i64, dp, dp, dp, dp, dp, i32]
             _lib = lib
     return _lib
 
@@ -217,3 +220,46 @@ def bwd_dkv_rows(Q, K, V, dO, LSE, D, scale: float, causal: bool, kv_rows, threa
                                        int(causal), pr, len(rows), pdk, pdv, threads),
            "bwd_dkv_rows")
     return dK, dV
+
+
+def _mask(bmask, Hq, Nq, Nk, bsize):
+    m = np.ascontiguousarray(np.asarray(bmask) != 0, dtype=np.uint8)
+    nqb, nkb = -(-Nq // bsize), -(-Nk // bsize)
+    if m.ndim == 2:
+        m = m[None]
+    if m.shape[1:] != (nqb, nkb) or m.shape[0] not in (1, Hq):
+        raise ValueError(f"block mask must be [1 or Hq, {nqb}, {nkb}], got {m.shape}")
+    return m, m.ctypes.data_as(ctypes.POINTER(ctypes.c_uint8)), m.shape[0]
+
+
+def fwd_masked(Q, K, V, scale: float, causal: bool, bmask, bsize: int = 128, threads: int = 0):
+    """Block-sparse forward: bmask [Hq or 1, ceil(Nq/bsize), ceil(Nk/bsize)], zero
+    entries remove the block's keys.  Returns (O, LSE)."""
+    B, Hq, Hkv, Nq, Nk, d = _shapes(Q, K, V)
+    m, pm, mh = _mask(bmask, Hq, Nq, Nk, bsize)
+    Q, pq = _d(Q)
+    K, pk = _d(K)
+    V, pv = _d(V)
+    O, po = _d(np.empty((B, Hq, Nq, d)))
+    L, pl = _d(np.empty((B, Hq, Nq)))
+    _check(_load().oracle_fwd_masked(pq, pk, pv, B, Hq, Hkv, Nq, Nk, d, scale, int(causal), pm, mh,
+                                     bsize, po, pl, threads), "fwd_masked")
+    return O, L
+
+
+def bwd_masked(Q, K, V, dO, scale: float, causal: bool, bmask, bsize: int = 128, threads: int = 0):
+    """Block-sparse backward.  Returns dict with dQ, dK, dV, O, LSE."""
+    B, Hq, Hkv, Nq, Nk, d = _shapes(Q, K, V)
+    m, pm, mh = _mask(bmask, Hq, Nq, Nk, bsize)
+    Q, pq = _d(Q)
+    K, pk = _d(K)
+    V, pv = _d(V)
+    dO, pdo = _d(dO)
+    dQ, pdq = _d(np.empty((B, Hq, Nq, d)))
+    dK, pdk = _d(np.empty((B, Hkv, Nk, d)))
+    dV, pdv = _d(np.empty((B, Hkv, Nk, d)))
+    O, po = _d(np.empty((B, Hq, Nq, d)))
+    L, pl = _d(np.empty((B, Hq, Nq)))
+    _check(_load().oracle_bwd_masked(pq, pk, pv, pdo, B, Hq, Hkv, Nq, Nk, d, scale, int(causal), pm, mh,
+                                     bsize, pdq, pdk, pdv, po, pl, threads), "bwd_masked")
+    return {"dQ": dQ, "dK": dK, "dV": dV, "O": O, "LSE": L}

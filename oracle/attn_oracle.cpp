@@ -79,8 +79,24 @@ struct Shape {
   int d;
   double scale;
   int causal;
+  // Block-sparse mask (NULL: none): bmask[hm][i / bsize][j / bsize] != 0
+  // keeps the block, hm = 0 when one mask serves every head, else the query
+  // head ("从Online-Softmax…" 0x04: Block-Sparse FlashAttention skips the
+  // masked blocks outright, i.e. their scores take no part in the softmax).
+  const uint8_t* bmask = nullptr;
+  int bmask_heads = 1;
+  int64_t bsize = 128;
   int group() const { return Hq / Hkv; }
 };
+
+// Does query i of query head h keep key j?  The causal rule, then the block mask.
+bool keep(const Shape& sh, int h, int64_t i, int64_t j) {
+  if (sh.causal && !oracle_causal_keep(i, j, sh.Nq, sh.Nk)) return false;
+  if (!sh.bmask) return true;
+  const int64_t nqb = (sh.Nq + sh.bsize - 1) / sh.bsize, nkb = (sh.Nk + sh.bsize - 1) / sh.bsize;
+  const int64_t hm = sh.bmask_heads == 1 ? 0 : h;
+  return sh.bmask[(hm * nqb + i / sh.bsize) * nkb + j / sh.bsize] != 0;
+}
 
 // One query row of the forward: fills s (scores of kept keys, Nk entries,
 // masked ones set to -inf), returns m and l, writes O (d) and LSE.
@@ -99,7 +115,7 @@ void fwd_row(const Shape& sh, const double* Q, const double* K, const double* V,
   // Pass 1: logits and their max.
   double m = kNegInf;
   for (int64_t j = 0; j < sh.Nk; ++j) {
-    if (sh.causal && !oracle_causal_keep(i, j, sh.Nq, sh.Nk)) continue;
+    if (!keep(sh, h, i, j)) continue;
     s[j] = sh.scale * dot(q, Kh + j * sh.d, sh.d);
     if (s[j] > m) m = s[j];
   }
@@ -170,7 +186,7 @@ void dkv_row(const Shape& sh, const double* Q, const double* K, const double* V,
     const int h = hk * G + g;
     const int64_t base = ((int64_t)b * sh.Hq + h) * sh.Nq;
     for (int64_t i = 0; i < sh.Nq; ++i) {
-      if (sh.causal && !oracle_causal_keep(i, j, sh.Nq, sh.Nk)) continue;
+      if (!keep(sh, h, i, j)) continue;
       const double lse = LSE[base + i];
       if (lse == kNegInf) continue;
       const double* qi = Q + (base + i) * sh.d;
@@ -373,6 +389,50 @@ int oracle_bwd_dkv_rows(const double* Q, const double* K, const double* V, const
   const Shape sh{B, Hq, Hkv, Nq, Nk, d, scale, causal};
   parallel_for(nrows, threads, [&](int64_t r) {
     dkv_row(sh, Q, K, V, dO, LSE, Dvec, kv_rows[r], dK_rows + r * d, dV_rows + r * d);
+  });
+  return 0;
+}
+
+int oracle_fwd_masked(const double* Q, const double* K, const double* V,
+                      int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                      double scale, int causal, const uint8_t* bmask, int bmask_heads, int64_t bsize,
+                      double* O, double* LSE, int threads) {
+  if (!Q || !K || !V || !O || !LSE || !bmask || bsize < 1 || bad_shape(B, Hq, Hkv, Nq, Nk, d) ||
+      (bmask_heads != 1 && bmask_heads != Hq))
+    return -1;
+  Shape sh{B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  sh.bmask = bmask;
+  sh.bmask_heads = bmask_heads;
+  sh.bsize = bsize;
+  const int64_t rows = (int64_t)B * Hq * Nq;
+  parallel_for(rows, threads, [&](int64_t r) {
+    thread_local std::vector<double> s;
+    fwd_row(sh, Q, K, V, r, s, O + r * d, LSE + r);
+  });
+  return 0;
+}
+
+int oracle_bwd_masked(const double* Q, const double* K, const double* V, const double* dO,
+                      int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                      double scale, int causal, const uint8_t* bmask, int bmask_heads, int64_t bsize,
+                      double* dQ, double* dK, double* dV, double* O, double* LSE, int threads) {
+  if (!Q || !K || !V || !dO || !dQ || !dK || !dV || !bmask || bsize < 1 ||
+      bad_shape(B, Hq, Hkv, Nq, Nk, d) || (bmask_heads != 1 && bmask_heads != Hq))
+    return -1;
+  Shape sh{B, Hq, Hkv, Nq, Nk, d, scale, causal};
+  sh.bmask = bmask;
+  sh.bmask_heads = bmask_heads;
+  sh.bsize = bsize;
+  const int64_t qrows = (int64_t)B * Hq * Nq;
+  const int64_t kvrows = (int64_t)B * Hkv * Nk;
+  std::vector<double> lse_buf(LSE ? 0 : (size_t)qrows), d_buf((size_t)qrows);
+  double* lse = LSE ? LSE : lse_buf.data();
+  parallel_for(qrows, threads, [&](int64_t r) {
+    thread_local std::vector<double> s, o;
+    dq_row(sh, Q, K, V, dO, r, s, o, dQ + r * d, lse + r, O ? O + r * d : nullptr, d_buf.data() + r);
+  });
+  parallel_for(kvrows, threads, [&](int64_t r) {
+    dkv_row(sh, Q, K, V, dO, lse, d_buf.data(), r, dK + r * d, dV + r * d);
   });
   return 0;
 }

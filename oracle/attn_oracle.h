@@ -99,6 +99,21 @@ int oracle_bwd_dkv_rows(const double* Q, const double* K, const double* V, const
                         double scale, int causal, const int64_t* kv_rows, int64_t nrows,
                         double* dK_rows, double* dV_rows, int threads);
 
+/* Block-sparse forward and backward: as oracle_fwd / oracle_bwd with a block
+ * mask on top of the causal rule.  bmask is uint8 [bmask_heads][ceil(Nq/bsize)]
+ * [ceil(Nk/bsize)] with bmask_heads 1 (one mask for every head) or Hq; a zero
+ * entry removes the block's keys from its queries' softmax ("从Online-Softmax…"
+ * 0x04, Block-Sparse FlashAttention skips masked blocks).  A row left with no
+ * key gives O = 0, LSE = -inf (and zero gradients). */
+int oracle_fwd_masked(const double* Q, const double* K, const double* V,
+                      int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                      double scale, int causal, const uint8_t* bmask, int bmask_heads, int64_t bsize,
+                      double* O, double* LSE, int threads);
+int oracle_bwd_masked(const double* Q, const double* K, const double* V, const double* dO,
+                      int B, int Hq, int Hkv, int64_t Nq, int64_t Nk, int d,
+                      double scale, int causal, const uint8_t* bmask, int bmask_heads, int64_t bsize,
+                      double* dQ, double* dK, double* dV, double* O, double* LSE, int threads);
+
 #ifdef __cplusplus
 }
 #endif
