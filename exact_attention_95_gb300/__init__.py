@@ -13,6 +13,9 @@ Functions carry the C names:
   and key lengths may differ (bottom-right causal alignment); the key range may
   be split, with the partial results merged
 * ``attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)``
+* ``attn_fwd_masked(Q, K, V, block_mask, scale, causal, out_dtype=None)`` and
+  ``attn_bwd_masked(Q, K, V, O, dO, LSE, block_mask, scale, causal)``: block-sparse
+  attention with a uint8 CUDA mask [1 or Hq, ceil(N/128), ceil(N/128)]
 * ``attn_bwd(Q, K, V, O, dO, LSE, scale, causal) -> (dQ, dK, dV)``
 * ``attn_bwd_workspace_size(B, Hq, Hkv, N, d)``
 * ``attn_last_device_status(stream=None)``, ``attn_status_string(code)``
@@ -38,7 +41,8 @@ ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5
 ATTN_BF16, ATTN_F32 = 0, 1
 
-EXPORTED = ("attn_fwd", "attn_fwd_split", "attn_fwd_split_workspace_size", "attn_bwd",
+EXPORTED = ("attn_fwd", "attn_fwd_split", "attn_fwd_split_workspace_size", "attn_fwd_masked",
+            "attn_bwd_masked", "attn_bwd",
             "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_convert", "attn_bwd_workspace_size",
             "attn_status_string", "attn_last_device_status", "attn_selftest_wait_timeout")
 _BWD_STAGES = {"all": "attn_bwd", "preprocess": "attn_bwd_preprocess", "main": "attn_bwd_main",
@@ -78,6 +82,11 @@ def load_library(path: str = LIB_PATH):
         lib.attn_fwd_split.restype = i32
         lib.attn_fwd_split_workspace_size.argtypes = [i32, i32, i32, i32, i32, i32, i32]
         lib.attn_fwd_split_workspace_size.restype = sz
+        lib.attn_fwd_masked.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, vp, i32, i32, vp]
+        lib.attn_fwd_masked.restype = i32
+        lib.attn_bwd_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
+                                        vp, i32, vp, sz, vp]
+        lib.attn_bwd_masked.restype = i32
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i32]
@@ -196,6 +205,69 @@ def attn_fwd_split(Q, K, V, scale=None, causal=False, num_splits=0, out_dtype=No
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_split")
     return O, LSE
+
+
+def _check_mask(block_mask, Hq, N):
+    T = (N + 127) // 128
+    if not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8:
+        raise TypeError("block_mask must be a uint8 CUDA tensor")
+    m = block_mask if block_mask.dim() == 3 else block_mask.reshape(1, T, T)
+    if tuple(m.shape[1:]) != (T, T) or m.shape[0] not in (1, Hq) or not m.is_contiguous():
+        raise ValueError(f"block_mask must be contiguous [1 or {Hq}, {T}, {T}], got {tuple(block_mask.shape)}")
+    return m, m.shape[0]
+
+
+def attn_fwd_masked(Q, K, V, block_mask, scale=None, causal=False, out_dtype=None, O=None, LSE=None,
+                    stream=None):
+    """Block-sparse forward: block_mask[h, i, j] == 0 removes the 128 x 128 block
+    (query tile i, key tile j) of head h (h = 0 for a mask shared by all heads)."""
+    lib = load_library()
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bf = torch.bfloat16
+    out_dtype = bf if out_dtype is None else out_dtype
+    out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
+    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv)):
+        _check_tensor(name, t, bf, (B, H, N, d))
+    m, mh = _check_mask(block_mask, Hq, N)
+    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Q.device) if O is None else O
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device) if LSE is None else LSE
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
+    rc = lib.attn_fwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, float(scale),
+                             int(bool(causal)), _ptr(m), mh, out_dt, _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_masked")
+    return O, LSE
+
+
+def attn_bwd_masked(Q, K, V, O, dO, LSE, block_mask, scale=None, causal=False, dQ=None, dK=None, dV=None,
+                    workspace=None, stream=None):
+    """Block-sparse backward with the mask of attn_fwd_masked."""
+    lib = load_library()
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    bf = torch.bfloat16
+    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv), ("O", O, Hq), ("dO", dO, Hq)):
+        _check_tensor(name, t, bf, (B, H, N, d))
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
+    m, mh = _check_mask(block_mask, Hq, N)
+    dQ = torch.empty_like(Q) if dQ is None else dQ
+    dK = torch.empty_like(K) if dK is None else dK
+    dV = torch.empty_like(V) if dV is None else dV
+    if workspace is None:
+        workspace = torch.empty(max(attn_bwd_workspace_size(B, Hq, Hkv, N, d), 1), dtype=torch.uint8,
+                                device=Q.device)
+    rc = lib.attn_bwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
+                             _ptr(dV), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), _ptr(m), mh,
+                             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_bwd_masked")
+    return dQ, dK, dV
 
 
 def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV=None,

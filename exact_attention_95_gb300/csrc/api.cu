@@ -169,12 +169,13 @@ size_t fwd_split_workspace_bytes(int B, int Hq, int Nq, int d, int splits) {
 // strides between splits.
 attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, float* LSE, int B, int Hq,
                          int Hkv, int Nq, int Nk, int d, float sl2, int causal, int out_f32, int splits,
-                         long long o_stride, long long lse_stride, cudaStream_t s) {
+                         long long o_stride, long long lse_stride, cudaStream_t s,
+                         const uint8_t* bmask = nullptr, int bmask_heads = 1) {
   int* status = status_ptr();
   if (!status) return ATTN_ERR_CUDA;
   // GQA packing when the whole group fits one 128-row tile (decoding).
   const int G = Hq / Hkv;
-  const bool packed = G > 1 && (long long)G * Nq <= 128;
+  const bool packed = G > 1 && (long long)G * Nq <= 128 && !bmask;  // masks may differ per head
   const long long heads = packed ? (long long)B * Hkv : (long long)B * Hq;
   const int rows = packed ? G * Nq : Nq;
   CUtensorMap tq, tk, tv;
@@ -183,6 +184,8 @@ attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, f
     return ATTN_ERR_CUDA;
   FwdParams p{};
   p.packed = packed ? 1 : 0;
+  p.bmask = bmask;
+  p.bmask_heads = bmask_heads;
   p.heads = (int)heads;
   p.rows = rows;
   p.O = O;
@@ -282,6 +285,21 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
+attn_status attn_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, int mask_heads, attn_dtype out_dtype, void* stream) {
+  if (!Q || !K || !V || !O || !LSE || !block_mask) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_BF16 && out_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(Q, 16) || !aligned(K, 16) || !aligned(V, 16) || !aligned(O, 16) || !aligned(LSE, 4))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_shape(B, Hq, Hkv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (mask_heads != 1 && mask_heads != Hq) return ATTN_ERR_INVALID_ARG;
+  if ((N + 127) / 128 > kMaxMaskTiles) return ATTN_ERR_UNSUPPORTED;
+  return fwd_bf16_run(Q, K, V, O, LSE, B, Hq, Hkv, N, N, d, scale * 1.4426950408889634f, causal,
+                      out_dtype == ATTN_F32, 1, 0, 0, static_cast<cudaStream_t>(stream), block_mask, mask_heads);
+}
+
 size_t attn_fwd_split_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {
   if (B < 1 || Hq < 1 || Hkv < 1 || Hq % Hkv != 0 || Nq < 1 || Nk < 1 || (d != 64 && d != 128)) return 0;
   const int splits = fwd_splits(B, Hq, Hkv, Nq, Nk, num_splits);
@@ -301,7 +319,8 @@ namespace {
 attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void* V,
                        const void* O, const void* dO, const float* LSE, void* dQ, void* dK,
                        void* dV, int B, int Hq, int Hkv, int N, int d, float scale, int causal,
-                       attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream) {
+                       attn_dtype dtype, void* workspace, size_t workspace_bytes, void* stream,
+                       const uint8_t* bmask = nullptr, int bmask_heads = 1) {
   if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV || !workspace)
     return ATTN_ERR_INVALID_ARG;
   if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
@@ -344,6 +363,8 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
   p.Hkv = Hkv;
   p.N = N;
   p.Npad = Npad;
+  p.bmask = bmask;
+  p.bmask_heads = bmask_heads;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.causal = causal;
@@ -362,6 +383,19 @@ attn_status bwd_stages(unsigned stages, const void* Q, const void* K, const void
 }  // namespace
 
 extern "C" {
+
+attn_status attn_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, int mask_heads, void* workspace,
+                            size_t workspace_bytes, void* stream) {
+  if (!block_mask || (mask_heads != 1 && mask_heads != Hq)) return ATTN_ERR_INVALID_ARG;
+  if (check_shape(B, Hq, Hkv, N, d, scale, causal) == ATTN_OK &&
+      (long long)(Hq / Hkv) * ((N + 127) / 128) > kMaxMaskIters)
+    return ATTN_ERR_UNSUPPORTED;
+  return bwd_stages(kBwdAll, Q, K, V, O, dO, LSE, dQ, dK, dV, B, Hq, Hkv, N, d, scale, causal, ATTN_BF16,
+                    workspace, workspace_bytes, stream, block_mask, mask_heads);
+}
 
 attn_status attn_bwd(const void* Q, const void* K, const void* V, const void* O,
                      const void* dO, const float* LSE, void* dQ, void* dK, void* dV,

@@ -95,7 +95,10 @@ struct Bwd {
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
-  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
+  static constexpr int OFF_NLIST = OFF_ABORT + 4;   // block-sparse: entries in the list
+  static constexpr int OFF_LIST = OFF_NLIST + 4;    // uint32 (g << 16 | query tile) per entry
+  static constexpr int SMEM_BYTES = OFF_LIST + 4 * kMaxMaskIters + 1024;
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per block");
   // TMEM columns
   static constexpr uint32_t TM_DV = 0;
   static constexpr uint32_t TM_DK = D;
@@ -162,7 +165,8 @@ __global__ void __launch_bounds__(256) bwd_pre_kernel(const BwdParams p) {
       for (int u = 1; u < kRowsPerWarp; ++u)
         if (lane == u) mine = dsum[u];
       p.negD[r0 + lane] = -mine;
-      p.negLSE2[r0 + lane] = i0 + lane < p.N ? -lse * 1.4426950408889634f : -INFINITY;
+      // A row with no kept key (LSE = -inf) gets probability 0, like a padded row.
+      p.negLSE2[r0 + lane] = (i0 + lane < p.N && lse != -INFINITY) ? -lse * 1.4426950408889634f : -INFINITY;
     }
     float4* acc = reinterpret_cast<float4*>(p.dQacc + r0 * D);
     for (int k = lane; k < kRowsPerWarp * D / 4; k += 32) acc[k] = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -261,7 +265,39 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   const int n_q = (p.N + kBQ - 1) / kBQ;
   const int i0 = p.causal ? (k0 / kBQ) : 0;  // first query tile that sees these keys
   const int per_head = n_q - i0;
-  const int T = G * per_head;  // inner iterations (>= 1 since k0 < N)
+  int T = G * per_head;  // inner iterations (>= 1 since k0 < N; may be 0 when masked)
+  // Block-sparse: the (query head g, query tile) pairs whose block with this
+  // key tile is kept, listed by the otherwise idle warp 3 (ballot compaction).
+  const bool masked = p.bmask != nullptr;
+  uint32_t* const tlist = reinterpret_cast<uint32_t*>(smem + C::OFF_LIST);
+  int* const nlist = reinterpret_cast<int*>(smem + C::OFF_NLIST);
+  if (masked && warp == 3) {
+    int count = 0;
+    for (int base = 0; base < T; base += 32) {
+      const int t = base + lane;
+      bool keep = false;
+      uint32_t e = 0;
+      if (t < T) {
+        const int g = t / per_head, it = i0 + (t - g * per_head);
+        const uint8_t* mh = p.bmask + (size_t)(p.bmask_heads == 1 ? 0 : hk * G + g) * n_q * n_q;
+        keep = mh[(size_t)it * n_q + jt] != 0;
+        e = ((uint32_t)g << 16) | (uint32_t)it;
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, keep);
+      if (keep) tlist[count + __popc(bal & ((1u << lane) - 1u))] = e;
+      count += __popc(bal);
+    }
+    if (lane == 0) *nlist = count;
+  }
+  auto tile_of = [&](int t, int& g, int& it) {
+    if (masked) {
+      g = (int)(tlist[t] >> 16);
+      it = (int)(tlist[t] & 0xffffu);
+    } else {
+      g = t / per_head;
+      it = i0 + (t - g * per_head);
+    }
+  };
 
   if (threadIdx.x == 0) {
     mbar_init(bar(C::B_KVFULL), 1);
@@ -295,6 +331,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const WaitCtx wc{abort_flag, p.status, p.wait_limit_ns};
+  if (masked) T = *nlist;
 
   if (warp < 4) {
     regs_dec<kRegsLow>();
@@ -313,8 +350,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       for (int t = 0; t < T; ++t) {
         const int s = t % C::STAGES;
         if (t >= C::STAGES && !mbar_wait(bar(C::B_STEMPTY + s), ((t / C::STAGES) & 1) ^ 1, wc)) break;
-        const int g = t / per_head;
-        const int it = i0 + (t - g * per_head);
+        int g, it;
+        tile_of(t, g, it);
         const int bhq = b * p.Hq + hk * G + g;
         const uint32_t st = stage(s);
         const uint32_t fb = bar(C::B_STFULL + s);
@@ -417,8 +454,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       // reduce and releases the stage once the reduces have read it.
       for (int t = 0; t < T; ++t) {
         const int s = t % C::STAGES;
-        const int g = t / per_head;
-        const int it = i0 + (t - g * per_head);
+        int g, it;
+        tile_of(t, g, it);
         const int bhq = b * p.Hq + hk * G + g;
         const uint32_t st = stage(s);
         bool ok = true;
@@ -455,8 +492,8 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     bool ok = true;
     for (int t = 0; t < T; ++t) {
       const int s = t % C::STAGES;
-      const int g = t / per_head;
-      const int it = i0 + (t - g * per_head);
+      int g, it;
+      tile_of(t, g, it);
       const int qh0 = it * kBQ + 64 * h;  // first query column of this half
       const int bhq = b * p.Hq + hk * G + g;
       const uint32_t st = stage(s);
@@ -555,8 +592,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     }
     // Epilogue: dV and scale * dK rows of this key tile; warpgroup h writes
     // head-dim columns [h*D/2, (h+1)*D/2).
-    if (ok && mbar_wait(bar(C::B_KVDONE), (T - 1) & 1, wc)) {
-      tc_fence_after();
+    // (A key tile that no kept block reaches writes zero dK and dV.)
+    const bool have = T > 0;
+    if (ok && (!have || mbar_wait(bar(C::B_KVDONE), (T - 1) & 1, wc))) {
+      if (have) tc_fence_after();
       const size_t row = (size_t)bhk * p.N + key;
 #pragma unroll
       for (int which = 0; which < 2; ++which) {
@@ -567,8 +606,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         for (int c = 0; c < D / 64; ++c) {
           const int col = h * (D / 2) + 32 * c;
           uint32_t o[32];
-          tmem_ld32(base + col, o);
-          tmem_ld_wait(o);
+          if (have) {
+            tmem_ld32(base + col, o);
+            tmem_ld_wait(o);
+          } else {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) o[i] = 0u;
+          }
           if (key_ok) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll

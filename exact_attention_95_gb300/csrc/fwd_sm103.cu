@@ -73,7 +73,9 @@ struct Fwd {
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
-  static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;  // + alignment slack
+  static constexpr int OFF_NLIST = OFF_ABORT + 4;           // block-sparse: entries in the tile list
+  static constexpr int OFF_LIST = OFF_NLIST + 4;            // uint16 per listed K/V tile
+  static constexpr int SMEM_BYTES = OFF_LIST + 2 * kMaxMaskTiles + 1024;  // + alignment slack
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t IDESC_O = idesc_bf16(kBM, D, false, true);
   static constexpr uint32_t TM_S = 0;    // one S buffer shared by both tiles (128 columns)
@@ -84,7 +86,7 @@ struct Fwd {
 // ONE: every CTA computes query tile 0 only (N <= 128: decoding and short
 // sequences), with its own MMA schedule; otherwise both tiles (a last pair
 // whose second tile has no row below N still computes it, on zero rows).
-template <int D, bool ONE>
+template <int D, bool ONE, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
@@ -120,8 +122,39 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int k_last = (p.packed ? p.N : min(q0 + 2 * kBM, p.N)) - 1 + p.kv_off;
     kt_end = k_last < 0 ? 0 : min(kt_end, k_last / kBN + 1);
   }
-  const int n_kv = max(0, kt_end - kt0);
+  int n_kv = max(0, kt_end - kt0);
   constexpr bool two = !ONE;
+  // Block-sparse: the K/V tiles of [kt0, kt_end) that either query tile keeps
+  // (mask entry nonzero and not right of its causal diagonal), as a list of
+  // entries kt | 0x8000 (tile 0 keeps it) | 0x4000 (tile 1 keeps it), built by
+  // the otherwise idle warp 3 with a ballot compaction.
+  constexpr bool masked = MASKED;  // p.bmask != NULL
+  uint16_t* const tlist = reinterpret_cast<uint16_t*>(smem + C::OFF_LIST);
+  int* const nlist = reinterpret_cast<int*>(smem + C::OFF_NLIST);
+  if (masked && warp == 3) {
+    const int nkt = (p.Nk + kBN - 1) / kBN;
+    const int qa = q0 / kBM;  // the pair's first query tile
+    const uint8_t* mh = p.bmask + (size_t)(p.bmask_heads == 1 ? 0 : h) * p.n_qtiles * nkt;
+    int count = 0;
+    for (int base = kt0; base < kt_end; base += 32) {
+      const int kt = base + lane;
+      uint32_t e = 0;
+      if (kt < kt_end) {
+        bool on0 = mh[(size_t)qa * nkt + kt] != 0;
+        bool on1 = two && qa + 1 < p.n_qtiles && mh[(size_t)(qa + 1) * nkt + kt] != 0;
+        if (p.causal) {
+          on0 = on0 && kt * kBN <= min(q0 + kBM, p.N) - 1 + p.kv_off;
+          on1 = on1 && kt * kBN <= min(q0 + 2 * kBM, p.N) - 1 + p.kv_off;
+        }
+        if (on0 || on1) e = (uint32_t)kt | (on0 ? 0x8000u : 0u) | (on1 ? 0x4000u : 0u);
+      }
+      const uint32_t bal = __ballot_sync(0xffffffffu, e != 0);
+      if (e) tlist[count + __popc(bal & ((1u << lane) - 1u))] = (uint16_t)e;
+      count += __popc(bal);
+    }
+    if (lane == 0) *nlist = count;
+  }
+  auto ktile = [&](int j) -> int { return masked ? (tlist[j] & 0x3FFF) : kt0 + j; };
   float* const o_out = p.out_f32 ? static_cast<float*>(p.O) + split * p.o_split_stride : nullptr;
   uint16_t* const o_out16 = p.out_f32 ? nullptr : static_cast<uint16_t*>(p.O);
   float* const lse_out = p.LSE + split * p.lse_split_stride;
@@ -150,6 +183,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  if (masked) n_kv = *nlist;
   const WaitCtx wc{abort_flag, p.status, p.wait_limit_ns};
 
   if (warp < 4) {
@@ -194,7 +228,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const CUtensorMap* m = v ? &tmV : &tmK;
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
-                      (kt0 + j) * kBN, bh_kv);
+                      ktile(j) * kBN, bh_kv);
       }
       // Drain: every issued copy must land before the CTA may exit.
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
@@ -313,7 +347,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     const bool active = t == 0 || two;  // tile 1 of a one-tile CTA has no rows
     for (int j = 0; j < (active ? n_kv : 0); ++j) {
-      const int k0 = (kt0 + j) * kBN;
+      const int k0 = ktile(j) * kBN;
+      const bool on = !masked || ((tlist[j] >> (15 - t)) & 1);  // this tile keeps the block
       if (!mbar_wait(bar(C::B_SFULL + t), j & 1, wc)) {
         ok = false;
         break;
@@ -331,8 +366,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive(bar(C::B_SFREE));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
-      if ((k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qc0 + p.kv_off)) {
-        const int lim = p.causal ? min(p.Nk - 1, qc + p.kv_off) : p.Nk - 1;
+      if (!on || (k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qc0 + p.kv_off)) {
+        const int lim = !on ? -1 : p.causal ? min(p.Nk - 1, qc + p.kv_off) : p.Nk - 1;
 #pragma unroll
         for (int c = 0; c < 4; ++c)
 #pragma unroll
@@ -477,11 +512,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D, bool ONE>
+template <int D, bool ONE, bool MASKED>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, cudaStream_t stream) {
   using C = Fwd<D>;
-  auto kern = fwd_bf16_kernel<D, ONE>;
+  auto kern = fwd_bf16_kernel<D, ONE, MASKED>;
   // setmaxnreg moves registers inside the launch allocation; refuse to launch
   // if the compiler gave the kernel a different per-thread count than assumed
   // (a larger split than the allocation would leave setmaxnreg.inc waiting).
@@ -508,11 +543,17 @@ size_t fwd_bf16_smem_bytes(int d) {
 
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {
-  const bool one = p.rows <= kBM;
-  if (d == 128) return one ? launch_one<128, true>(tmQ, tmK, tmV, p, stream)
-                           : launch_one<128, false>(tmQ, tmK, tmV, p, stream);
-  if (d == 64) return one ? launch_one<64, true>(tmQ, tmK, tmV, p, stream)
-                          : launch_one<64, false>(tmQ, tmK, tmV, p, stream);
+  const bool one = p.rows <= kBM, m = p.bmask != nullptr;
+  if (d == 128)
+    return one ? (m ? launch_one<128, true, true>(tmQ, tmK, tmV, p, stream)
+                    : launch_one<128, true, false>(tmQ, tmK, tmV, p, stream))
+               : (m ? launch_one<128, false, true>(tmQ, tmK, tmV, p, stream)
+                    : launch_one<128, false, false>(tmQ, tmK, tmV, p, stream));
+  if (d == 64)
+    return one ? (m ? launch_one<64, true, true>(tmQ, tmK, tmV, p, stream)
+                    : launch_one<64, true, false>(tmQ, tmK, tmV, p, stream))
+               : (m ? launch_one<64, false, true>(tmQ, tmK, tmV, p, stream)
+                    : launch_one<64, false, false>(tmQ, tmK, tmV, p, stream));
   return cudaErrorInvalidValue;
 }
 

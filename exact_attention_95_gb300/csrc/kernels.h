@@ -23,6 +23,10 @@ struct FwdParams {
   // share one tile, whose row r is query r % N of head r / N of the group
   // (the heads of a group are adjacent, so their rows are contiguous).
   int packed;
+  // Block-sparse mask (NULL: dense): uint8 [bmask_heads][n_qtiles][ceil(Nk/128)],
+  // bmask_heads 1 or Hq; zero entries skip the 128 x 128 tile.
+  const uint8_t* bmask;
+  int bmask_heads;
   int heads;        // grid heads: B * Hq, or B * Hkv when packed
   int rows;         // rows per grid head: N, or G * N when packed
   int n_qtiles;     // ceil(rows / 128)
@@ -39,6 +43,7 @@ struct FwdParams {
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
 size_t fwd_bf16_smem_bytes(int d);
+constexpr int kMaxMaskTiles = 2048;  // key tiles a block-sparse forward may list per CTA
 
 // Merge of a split forward's partial results: Opart [n_splits][rows][d] fp32
 // (each normalised over its part), Lpart [n_splits][rows] fp32 (natural log)
@@ -71,7 +76,11 @@ struct BwdParams {
   int causal;
   int head_group;       // kv heads whose CTAs are launched together (L2 reuse)
   unsigned long long wait_limit_ns;
+  // Block-sparse mask (NULL: dense), as FwdParams::bmask with Nk = N.
+  const uint8_t* bmask;
+  int bmask_heads;
 };
+constexpr int kMaxMaskIters = 4096;  // (query head, query tile) pairs a masked backward CTA may list
 
 // Query rows are padded to a multiple of this in the backward workspace.
 int bwd_row_padding();

@@ -107,6 +107,33 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
                            attn_dtype out_dtype, int num_splits, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/*
+ * Block-sparse forward: attn_fwd with a block mask on top of the causal rule
+ * (Block-Sparse FlashAttention, "从Online-Softmax…" 0x04: the masked blocks
+ * are skipped outright, i.e. their keys take no part in the softmax).
+ *   block_mask: device pointer, uint8 [mask_heads][T][T] with T = ceil(N / 128)
+ *     (query tile, key tile); mask_heads 1 (one mask for every head) or Hq;
+ *     a zero entry removes the 128 x 128 block.  T <= 2048.
+ *   A query row whose blocks are all removed gets O = 0 and LSE = -inf.
+ * Other arguments as attn_fwd with bf16 input.
+ */
+attn_status attn_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, int mask_heads, attn_dtype out_dtype, void* stream);
+
+/*
+ * Block-sparse backward: attn_bwd with the block mask of attn_fwd_masked
+ * (same layout and meaning); LSE must come from attn_fwd_masked with the same
+ * mask.  Blocks the mask removes contribute nothing to dQ, dK, dV; a key row
+ * that no kept block reaches gets dK = dV = 0.  (Hq / Hkv) * ceil(N / 128)
+ * <= 4096.  Workspace and other arguments as attn_bwd (bf16).
+ */
+attn_status attn_bwd_masked(const void* Q, const void* K, const void* V, const void* O,
+                            const void* dO, const float* LSE, void* dQ, void* dK, void* dV,
+                            int B, int Hq, int Hkv, int N, int d, float scale, int causal,
+                            const uint8_t* block_mask, int mask_heads, void* workspace,
+                            size_t workspace_bytes, void* stream);
+
 /* Bytes of workspace attn_fwd_split needs for these sizes and num_splits
  * (0 when the key range is not split); 0 on bad sizes. */
 size_t attn_fwd_split_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits);

@@ -154,3 +154,31 @@ def test_fwd_split_argument_errors(lib):
     need = pkg.attn_fwd_split_workspace_size(1, 2, 1, 16, 1024, 64, 4)
     assert _fwd_split(lib, ws=A, wsb=need - 1) == pkg.ATTN_ERR_INVALID_ARG
     assert _fwd_split(lib, ws=ctypes.c_void_p(0x10010), wsb=need) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_masked_argument_errors(lib):
+    M = ctypes.c_void_p(0x20000)
+
+    def fwd(**kw):
+        a = dict(Q=A, K=A, V=A, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=256, d=64, scale=0.125, causal=1, m=M, mh=1,
+                 outd=0)
+        a.update(kw)
+        return lib.attn_fwd_masked(a["Q"], a["K"], a["V"], a["O"], a["LSE"], a["B"], a["Hq"], a["Hkv"], a["N"],
+                                   a["d"], a["scale"], a["causal"], a["m"], a["mh"], a["outd"], None)
+
+    assert fwd(m=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(mh=3) == pkg.ATTN_ERR_INVALID_ARG  # 1 or Hq
+    assert fwd(Q=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(d=96) == pkg.ATTN_ERR_UNSUPPORTED
+    assert fwd(N=128 * 2049) == pkg.ATTN_ERR_UNSUPPORTED  # more key tiles than a CTA may list
+
+    def bwd(**kw):
+        a = dict(B=1, Hq=2, Hkv=1, N=256, d=64, m=M, mh=2, ws=A, wsb=1 << 30)
+        a.update(kw)
+        return lib.attn_bwd_masked(A, A, A, A, A, A, A, A, A, a["B"], a["Hq"], a["Hkv"], a["N"], a["d"], 0.125, 1,
+                                   a["m"], a["mh"], a["ws"], a["wsb"], None)
+
+    assert bwd(m=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(mh=5) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(ws=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert bwd(Hq=64, Hkv=1, N=128 * 65, mh=1) == pkg.ATTN_ERR_UNSUPPORTED  # 64 x 65 > 4096 pairs
