@@ -270,6 +270,8 @@ def run_native(args):
     pkg.load_library()
     if args.workload == "decode":
         return run_decode(args, pkg, rank, world, dev)
+    if args.workload == "sparse":
+        return run_sparse(args, pkg, rank, world, dev)
     w = inputs.WORKLOADS[args.workload]
     if w.dtype != "bf16" or not w.backward:
         return run_fwd_only(args, w, pkg, rank, world, dev)
@@ -591,6 +593,96 @@ def run_decode(args, pkg, rank, world, dev):
                 "h2d_bytes_per_step": sum(t.numel() * 2 for t in (hQ, hK, hV)),
                 "d2h_bytes_per_step": hO.numel() * 2},
         "gpu_launches": 2 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_sparse(args, pkg, rank, world, dev):
+    """Block-sparse step (attn_fwd_masked + attn_bwd_masked) on the c3 tensors
+    with a seeded random block mask of density 1/2 shared by all heads.  FLOPs
+    count the kept scores only (causal and mask); the dense step on the same
+    tensors is timed alongside."""
+    import numpy as np
+    import torch
+    from exact_attention_95_gb300 import inputs
+
+    w = inputs.WORKLOADS["c3"]
+    t_np = inputs.workload_tensors(w)
+    Q, K, V, dO = (torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).to(dev)
+                   for k in ("Q", "K", "V", "dO"))
+    T = (w.N + 127) // 128
+    mask_np = (np.random.default_rng(0x5EED).random((1, T, T)) < 0.5).astype(np.uint8)
+    mask = torch.from_numpy(mask_np).to(dev)
+    # Kept scores per head: causal lower triangle restricted to kept blocks.
+    idx = np.arange(w.N)
+    kept = 0
+    for qi in range(T):
+        rows = idx[qi * 128:(qi + 1) * 128]
+        for kj in range(T):
+            if mask_np[0, qi, kj]:
+                cols = idx[kj * 128:(kj + 1) * 128]
+                kept += int((cols[None, :] <= rows[:, None]).sum())
+    fwd_flops = 4.0 * kept * w.d * w.Hq * w.B
+    stream = torch.cuda.current_stream()
+    O = torch.empty_like(Q)
+    L = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    ws = torch.empty(pkg.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8, device=dev)
+    bufs = [torch.empty_like(Q), torch.empty_like(K), torch.empty_like(V)]
+
+    def sparse_step():
+        pkg.attn_fwd_masked(Q, K, V, mask, w.scale, w.causal, O=O, LSE=L, stream=stream)
+        pkg.attn_bwd_masked(Q, K, V, O, dO, L, mask, w.scale, w.causal, *bufs, workspace=ws, stream=stream)
+
+    def dense_step():
+        pkg.attn_fwd(Q, K, V, w.scale, w.causal, O=O, LSE=L, stream=stream)
+        pkg.attn_bwd(Q, K, V, O, dO, L, w.scale, w.causal, *bufs, ws, stream)
+
+    def timed(step, steps):
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        if pkg.attn_last_device_status() != pkg.ATTN_OK:
+            raise RuntimeError("device status not OK")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(dev.index)
+    barrier()
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        ms = timed(sparse_step, args.steps)
+        wall = time.perf_counter() - wall0
+    ms_dense = timed(dense_step, max(3, args.steps // 4))
+    ms = max_over_ranks(ms, dev)
+    flops = 3.5 * fwd_flops
+    value = flops * world / (ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    sustained = float(peaks.get("bf16_tflops_sustained", FALLBACK_PEAK["bf16_tflops_sustained"]))
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded iid N(0,1), bf16)",
+        "config": {"workload": "sparse: c3 tensors (B2 H32 N4096 d128 causal, Q x8) with a random block "
+                               "mask of density 1/2 shared by all heads; FLOPs of kept scores only",
+                   "mask_blocks_kept": int(mask_np.sum()), "mask_blocks": int(T * T),
+                   "l2": "working set larger than the 126 MiB L2; no flush",
+                   "parallelism": f"replicas x{world} (weak)"},
+        "step": {"ms": ms, "ms_dense_same_tensors": ms_dense, "speedup_vs_dense": ms_dense / ms},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": sustained, "unit": "TFLOP/s",
+                     "frac": value / world / sustained, "traffic": None,
+                     "kernel": "whole masked step (fwd + bwd)", "peak_source": f"bf16_tflops_sustained of {peak_src}"},
+        "gpu_launches": 4 * args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }
