@@ -13,7 +13,9 @@ readings taken here:
     infinities.
   - Rounding to nearest, ties to even; values beyond 448 saturate to +-448.
   - A block is 128 consecutive rows of one head; its scale is amax / 448
-    (1 for an all-zero block), and x is stored as e4m3(x / scale).
+    (1 for an all-zero block), and x is stored as e4m3(x / scale).  The
+    division and the scale are fp32 operations (IEEE, round to nearest), as
+    in the kernel that produces the codes, so both round the same quotient.
 """
 
 import numpy as np
@@ -68,17 +70,18 @@ def quantize_blocks(x, transpose=False):
     """Block quantization of x [BH, N, d] (float64): per 128-row block of a head,
     scale = amax / 448 (1 if the block is zero) and codes = e4m3(x / scale).
     Returns (codes [BH, N, d] or, with transpose, [BH, d, N]; scales [BH, T])."""
-    x = np.asarray(x, dtype=np.float64)
+    x = np.asarray(x, dtype=np.float32)
     BH, N, d = x.shape
     T = -(-N // BLOCK)
-    scales = np.ones((BH, T))
+    scales = np.ones((BH, T), dtype=np.float32)
     codes = np.zeros((BH, N, d), dtype=np.uint8)
     for t in range(T):
         blk = x[:, t * BLOCK:(t + 1) * BLOCK, :]
         amax = np.abs(blk).max(axis=(1, 2))
-        sc = np.where(amax > 0, amax / E4M3_MAX, 1.0)
+        sc = np.where(amax > 0, amax / np.float32(E4M3_MAX), np.float32(1.0)).astype(np.float32)
         scales[:, t] = sc
-        codes[:, t * BLOCK:(t + 1) * BLOCK, :] = encode_e4m3(round_e4m3(blk / sc[:, None, None]))
+        q = (blk / sc[:, None, None]).astype(np.float32)  # fp32 quotient, round to nearest
+        codes[:, t * BLOCK:(t + 1) * BLOCK, :] = encode_e4m3(round_e4m3(q.astype(np.float64)))
     if transpose:
         codes = np.ascontiguousarray(codes.transpose(0, 2, 1))
     return codes, scales
