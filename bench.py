@@ -270,6 +270,8 @@ def run_native(args):
     pkg.load_library()
     if args.workload == "decode":
         return run_decode(args, pkg, rank, world, dev)
+    if args.workload == "fp8":
+        return run_fp8(args, pkg, rank, world, dev)
     if args.workload == "sparse":
         return run_sparse(args, pkg, rank, world, dev)
     w = inputs.WORKLOADS[args.workload]
@@ -683,6 +685,110 @@ def run_sparse(args, pkg, rank, world, dev):
                      "frac": value / world / sustained, "traffic": None,
                      "kernel": "whole masked step (fwd + bwd)", "peak_source": f"bf16_tflops_sustained of {peak_src}"},
         "gpu_launches": 4 * args.steps,
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_fp8(args, pkg, rank, world, dev):
+    """FP8 (e4m3, per-128-row-block scales) forward on the c3 tensors: Q, K and
+    V quantized once by attn_quantize_fp8 (V transposed), then attn_fwd_fp8
+    timed.  The bf16 forward on the same tensors and the quantizer are timed
+    alongside; e2e covers H2D of the bf16 inputs, quantization, the forward
+    and D2H of O."""
+    import numpy as np
+    import torch
+    from exact_attention_95_gb300 import inputs
+
+    w = inputs.WORKLOADS["c3"]
+    t_np = inputs.workload_tensors(w, names=("Q", "K", "V"))
+    Q, K, V = (torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).to(dev) for k in ("Q", "K", "V"))
+    stream = torch.cuda.current_stream()
+    qc, qs = pkg.attn_quantize_fp8(Q, stream=stream)
+    kc, ks = pkg.attn_quantize_fp8(K, stream=stream)
+    vc, vs = pkg.attn_quantize_fp8(V, transpose=True, stream=stream)
+    O = torch.empty_like(Q)
+    L = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+
+    def fp8_step():
+        pkg.attn_fwd_fp8(qc, qs, kc, ks, vc, vs, w.scale, w.causal, O=O, LSE=L, stream=stream)
+
+    def bf16_step():
+        pkg.attn_fwd(Q, K, V, w.scale, w.causal, O=O, LSE=L, stream=stream)
+
+    def quant_step():
+        pkg.attn_quantize_fp8(Q, codes=qc, scales=qs, stream=stream)
+        pkg.attn_quantize_fp8(K, codes=kc, scales=ks, stream=stream)
+        pkg.attn_quantize_fp8(V, transpose=True, codes=vc, scales=vs, stream=stream)
+
+    def timed(step, steps):
+        for _ in range(max(3, args.warmup)):
+            step()
+        torch.cuda.synchronize()
+        if pkg.attn_last_device_status() != pkg.ATTN_OK:
+            raise RuntimeError("device status not OK")
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(steps):
+            step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / steps
+
+    props = torch.cuda.get_device_properties(dev)
+    uuid = getattr(props, "uuid", None)
+    gpu_id = f"GPU-{uuid}" if uuid is not None else str(dev.index)
+    barrier()
+    with ClockSampler(gpu_id) as clk:
+        wall0 = time.perf_counter()
+        ms = timed(fp8_step, args.steps)
+        wall = time.perf_counter() - wall0
+    ms_bf16 = timed(bf16_step, max(3, args.steps // 2))
+    ms_quant = timed(quant_step, max(3, args.steps // 4))
+    ms = max_over_ranks(ms, dev)
+    flops = w.fwd_flops()
+    value = flops * world / (ms / 1e3) / 1e12
+    peaks, peak_src = load_peaks()
+    fp8_peak = 2.0 * float(peaks.get("bf16_tflops", FALLBACK_PEAK["bf16_tflops"]))
+    elems = sum(t.numel() for t in (Q, K, V))
+    q_bytes = 3 * elems + 4 * sum(t.numel() for t in (qs, ks, vs)) + (vc.numel() - V.numel())
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAK["hbm_gbs"]))
+
+    # e2e: pinned host bf16 inputs -> device, quantize, forward, O back to the host.
+    host = {k: torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in ("Q", "K", "V")}
+    hout = torch.empty(O.shape, dtype=torch.bfloat16).pin_memory()
+
+    def e2e_step():
+        Q.copy_(host["Q"], non_blocking=True)
+        K.copy_(host["K"], non_blocking=True)
+        V.copy_(host["V"], non_blocking=True)
+        quant_step()
+        fp8_step()
+        hout.copy_(O, non_blocking=True)
+
+    ms_e2e = timed(e2e_step, max(1, args.e2e_steps))
+    line = {
+        "metric": "attention fwd TFLOPS (fp8 e4m3 with per-block scales, causal, N=4K, d=128)",
+        "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "e4m3", "data": "synthetic (seeded iid N(0,1), bf16, quantized to e4m3)",
+        "config": {"workload": "fp8: c3 tensors (B2 H32 N4096 d128 causal, Q x8), forward only, "
+                               "quantized once per 128-row block (not in the timed region)",
+                   "l2": "working set (fp8 Q,K,V 100 MB + bf16 O 67 MB) above the 126 MiB L2; no flush",
+                   "parallelism": f"replicas x{world} (weak)"},
+        "step": {"ms_fp8_fwd": ms, "ms_bf16_fwd_same_tensors": ms_bf16, "speedup_vs_bf16": ms_bf16 / ms,
+                 "ms_quantize_qkv": ms_quant,
+                 "quantize_hbm_frac": q_bytes / (ms_quant / 1e3) / 1e9 / hbm},
+        "roofline": {"bound": "tensor", "achieved": value / world, "peak": fp8_peak, "unit": "TFLOP/s",
+                     "frac": value / world / fp8_peak, "traffic": None, "kernel": "fwd_fp8_kernel",
+                     "peak_source": f"2 x bf16_tflops of {peak_src} (nominal fp8:bf16 dense ratio 4.5:2.25)"},
+        "e2e": {"value": flops * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms_e2e,
+                "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
+                "d2h_bytes_per_step": hout.numel() * hout.element_size()},
+        "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }

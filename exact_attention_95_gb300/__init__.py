@@ -42,7 +42,7 @@ ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5
 ATTN_BF16, ATTN_F32 = 0, 1
 
 EXPORTED = ("attn_fwd", "attn_fwd_split", "attn_fwd_split_workspace_size", "attn_fwd_masked",
-            "attn_bwd_masked", "attn_bwd",
+            "attn_bwd_masked", "attn_quantize_fp8", "attn_fp8_vt_stride", "attn_fwd_fp8", "attn_bwd",
             "attn_bwd_preprocess", "attn_bwd_main", "attn_bwd_convert", "attn_bwd_workspace_size",
             "attn_status_string", "attn_last_device_status", "attn_selftest_wait_timeout")
 _BWD_STAGES = {"all": "attn_bwd", "preprocess": "attn_bwd_preprocess", "main": "attn_bwd_main",
@@ -87,6 +87,12 @@ def load_library(path: str = LIB_PATH):
         lib.attn_bwd_masked.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32,
                                         vp, i32, vp, sz, vp]
         lib.attn_bwd_masked.restype = i32
+        lib.attn_fp8_vt_stride.argtypes = [i32]
+        lib.attn_fp8_vt_stride.restype = i32
+        lib.attn_quantize_fp8.argtypes = [vp, vp, vp, ctypes.c_longlong, i32, i32, i32, vp]
+        lib.attn_quantize_fp8.restype = i32
+        lib.attn_fwd_fp8.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
+        lib.attn_fwd_fp8.restype = i32
         lib.attn_bwd_workspace_size.argtypes = [i32, i32, i32, i32, i32]
         lib.attn_bwd_workspace_size.restype = sz
         lib.attn_status_string.argtypes = [i32]
@@ -240,6 +246,61 @@ def attn_fwd_masked(Q, K, V, block_mask, scale=None, causal=False, out_dtype=Non
                              int(bool(causal)), _ptr(m), mh, out_dt, _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_masked")
+    return O, LSE
+
+
+def attn_fp8_vt_stride(N: int) -> int:
+    """Row length of transposed FP8 codes: N rounded up to 16."""
+    return int(load_library().attn_fp8_vt_stride(int(N)))
+
+
+def attn_quantize_fp8(X, transpose=False, codes=None, scales=None, stream=None):
+    """Per-128-row-block e4m3 quantization of X [B, H, N, d] (bf16).
+
+    Returns (codes, scales): codes uint8 [B, H, N, d], or with transpose
+    [B, H, d, attn_fp8_vt_stride(N)]; scales fp32 [B, H, ceil(N / 128)]."""
+    lib = load_library()
+    B, H, N, d = X.shape
+    _check_tensor("X", X, torch.bfloat16, (B, H, N, d))
+    T = (N + 127) // 128
+    cshape = (B, H, d, attn_fp8_vt_stride(N)) if transpose else (B, H, N, d)
+    codes = torch.empty(cshape, dtype=torch.uint8, device=X.device) if codes is None else codes
+    scales = torch.empty((B, H, T), dtype=torch.float32, device=X.device) if scales is None else scales
+    _check_tensor("codes", codes, torch.uint8, cshape)
+    _check_tensor("scales", scales, torch.float32, (B, H, T))
+    rc = lib.attn_quantize_fp8(_ptr(X), _ptr(codes), _ptr(scales), B * H, N, d, int(bool(transpose)),
+                               _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_quantize_fp8")
+    return codes, scales
+
+
+def attn_fwd_fp8(Qc, q_scale, Kc, k_scale, Vtc, v_scale, scale=None, causal=False, out_dtype=None, O=None,
+                 LSE=None, stream=None):
+    """FP8 forward on block-quantized Q, K and transposed V (see attn_quantize_fp8)."""
+    lib = load_library()
+    B, Hq, N, d = Qc.shape
+    Hkv = Kc.shape[1]
+    T = (N + 127) // 128
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    out_dtype = torch.bfloat16 if out_dtype is None else out_dtype
+    out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
+    u8, f32 = torch.uint8, torch.float32
+    _check_tensor("Qc", Qc, u8, (B, Hq, N, d))
+    _check_tensor("Kc", Kc, u8, (B, Hkv, N, d))
+    _check_tensor("Vtc", Vtc, u8, (B, Hkv, d, attn_fp8_vt_stride(N)))
+    _check_tensor("q_scale", q_scale, f32, (B, Hq, T))
+    _check_tensor("k_scale", k_scale, f32, (B, Hkv, T))
+    _check_tensor("v_scale", v_scale, f32, (B, Hkv, T))
+    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Qc.device) if O is None else O
+    LSE = torch.empty((B, Hq, N), dtype=f32, device=Qc.device) if LSE is None else LSE
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
+    _check_tensor("LSE", LSE, f32, (B, Hq, N))
+    rc = lib.attn_fwd_fp8(_ptr(Qc), _ptr(q_scale), _ptr(Kc), _ptr(k_scale), _ptr(Vtc), _ptr(v_scale), _ptr(O),
+                          _ptr(LSE), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), out_dt, _stream(stream))
+    if rc != ATTN_OK:
+        raise AttnError(rc, "attn_fwd_fp8")
     return O, LSE
 
 

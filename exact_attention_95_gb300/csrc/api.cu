@@ -81,13 +81,28 @@ bool make_acc_map(CUtensorMap* m, const void* base, long long rows, int d) {
             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over uint8 e4m3 codes [planes][rows][cols] (row stride `ld` bytes):
+// box of 128 bytes x 128 rows x 1 plane, 128-byte swizzle.  Reads past the
+// extents return zero.
+bool make_map_u8(CUtensorMap* m, const void* base, long long planes, int rows, int cols, long long ld) {
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)ld * rows};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 // Shape checks shared by forward and backward.  Returns ATTN_OK or an error.
 attn_status check_shape(int B, int Hq, int Hkv, int N, int d, float scale, int causal) {
   if (B < 1 || Hq < 1 || Hkv < 1 || N < 1 || d < 1) return ATTN_ERR_INVALID_ARG;
   if (Hq % Hkv != 0) return ATTN_ERR_INVALID_ARG;
-  if (!std::isfinite(scale)) return ATTN_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return ATTN_ERR_INVALID_ARG;
   if (causal != 0 && causal != 1) return ATTN_ERR_INVALID_ARG;
   if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
   // Grid limits: query tiles on grid.y, (b, h) on grid.x; element counts fit int64.
@@ -298,6 +313,62 @@ attn_status attn_fwd_masked(const void* Q, const void* K, const void* V, void* O
   if ((N + 127) / 128 > kMaxMaskTiles) return ATTN_ERR_UNSUPPORTED;
   return fwd_bf16_run(Q, K, V, O, LSE, B, Hq, Hkv, N, N, d, scale * 1.4426950408889634f, causal,
                       out_dtype == ATTN_F32, 1, 0, 0, static_cast<cudaStream_t>(stream), block_mask, mask_heads);
+}
+
+int attn_fp8_vt_stride(int N) { return N < 1 ? 0 : (N + 15) / 16 * 16; }
+
+attn_status attn_quantize_fp8(const void* X, void* codes, float* scales, long long BH, int N, int d,
+                              int transpose, void* stream) {
+  if (!X || !codes || !scales) return ATTN_ERR_INVALID_ARG;
+  if (BH < 1 || N < 1 || (transpose != 0 && transpose != 1)) return ATTN_ERR_INVALID_ARG;
+  if (d != 64 && d != 128) return ATTN_ERR_UNSUPPORTED;
+  if (!aligned(X, 16) || !aligned(codes, 16) || !aligned(scales, 4)) return ATTN_ERR_INVALID_ARG;
+  cudaError_t e = launch_quantize_fp8(d, static_cast<const uint16_t*>(X), static_cast<uint8_t*>(codes), scales, BH,
+                                      N, transpose, attn_fp8_vt_stride(N), static_cast<cudaStream_t>(stream));
+  if (e == cudaErrorInvalidValue) return ATTN_ERR_UNSUPPORTED;
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
+}
+
+attn_status attn_fwd_fp8(const void* Qc, const float* q_scale, const void* Kc, const float* k_scale,
+                         const void* Vtc, const float* v_scale, void* O, float* LSE, int B, int Hq, int Hkv,
+                         int N, int d, float scale, int causal, attn_dtype out_dtype, void* stream) {
+  if (!Qc || !q_scale || !Kc || !k_scale || !Vtc || !v_scale || !O || !LSE) return ATTN_ERR_INVALID_ARG;
+  if (out_dtype != ATTN_BF16 && out_dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  if (!aligned(Qc, 16) || !aligned(Kc, 16) || !aligned(Vtc, 16) || !aligned(O, 16) || !aligned(LSE, 4) ||
+      !aligned(q_scale, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+    return ATTN_ERR_INVALID_ARG;
+  attn_status st = check_shape(B, Hq, Hkv, N, d, scale, causal);
+  if (st != ATTN_OK) return st;
+  if (d != 128) return ATTN_ERR_UNSUPPORTED;
+  int* status = status_ptr();
+  if (!status) return ATTN_ERR_CUDA;
+  const int ldt = attn_fp8_vt_stride(N);
+  CUtensorMap tq, tk, tv;
+  if (!make_map_u8(&tq, Qc, (long long)B * Hq, N, 128, 128) || !make_map_u8(&tk, Kc, (long long)B * Hkv, N, 128, 128) ||
+      !make_map_u8(&tv, Vtc, (long long)B * Hkv, 128, ldt, ldt))
+    return ATTN_ERR_CUDA;
+  Fp8FwdParams p{};
+  p.sq = q_scale;
+  p.sk = k_scale;
+  p.sv = v_scale;
+  p.O = O;
+  p.LSE = LSE;
+  p.status = status;
+  p.B = B;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.N = N;
+  p.T = (N + 127) / 128;
+  p.heads = B * Hq;
+  p.n_pairs = (p.T + 1) / 2;
+  if ((long long)p.heads * p.n_pairs > 0x7fffffffLL) return ATTN_ERR_UNSUPPORTED;
+  p.head_group = head_group_for((size_t)N * 128 * 2, p.heads, size_t(64) << 20);
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.causal = causal;
+  p.out_f32 = out_dtype == ATTN_F32;
+  p.wait_limit_ns = wait_limit();
+  cudaError_t e = launch_fwd_fp8(tq, tk, tv, p, static_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 
 size_t attn_fwd_split_workspace_size(int B, int Hq, int Hkv, int Nq, int Nk, int d, int num_splits) {

@@ -51,6 +51,32 @@ constexpr int kMaxMaskTiles = 2048;  // key tiles a block-sparse forward may lis
 cudaError_t launch_fwd_merge(int d, const float* Opart, const float* Lpart, void* O, float* LSE, long long rows,
                              int n_splits, int out_f32, cudaStream_t stream);
 
+// FP8 (e4m3) forward, d = 128, Nq = Nk = N.  tmQ/tmK: 3-D uint8 maps over
+// [B*H][N][128] codes; tmVt over the transposed V codes [B*Hkv][128][Npad];
+// all with a (128, 128, 1) box and 128-byte swizzle.
+struct Fp8FwdParams {
+  const float* sq;  // [B*Hq][T] block scales of Q (T = ceil(N / 128))
+  const float* sk;  // [B*Hkv][T]
+  const float* sv;  // [B*Hkv][T]
+  void* O;          // [B, Hq, N, 128] bf16 or fp32
+  float* LSE;       // [B, Hq, N]
+  int* status;
+  int B, Hq, Hkv, N, T;
+  int heads;        // B * Hq
+  int n_pairs;      // ceil(T / 2)
+  int head_group;
+  float scale_log2;
+  int causal;
+  int out_f32;
+  unsigned long long wait_limit_ns;
+};
+cudaError_t launch_fwd_fp8(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmVt,
+                           const Fp8FwdParams& p, cudaStream_t stream);
+// Block quantizer: X bf16 [BH][N][d] -> codes ([BH][N][d], or [BH][d][ldt]
+// when transposed) and scales [BH][ceil(N / 128)].
+cudaError_t launch_quantize_fp8(int d, const uint16_t* X, uint8_t* codes, float* scales, long long BH, int N,
+                                int transpose, int ldt, cudaStream_t stream);
+
 // fp32 SIMT forward (exact fp32 arithmetic, FFMA + ex2).
 cudaError_t launch_fwd_f32(int d, const float* Q, const float* K, const float* V, float* O,
                            float* LSE, int B, int Hq, int Hkv, int N, float scale_log2,

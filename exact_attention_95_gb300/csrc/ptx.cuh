@@ -164,6 +164,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn_major,
          ((b_mn_major ? 1u : 0u) << 16) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
 }
 
+// Instruction descriptor for kind::f8f6f4 with e4m3 A and B (format code 0
+// for both) and fp32 accumulation; both operands K-major.  Same bit layout.
+__host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
+  return (1u << 4) | ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
 // Shared-memory matrix descriptor, 128-byte swizzle.  Bits: [0,14) address>>4,
 // [16,30) leading byte offset>>4, [32,46) stride byte offset>>4, [46,48) = 1,
 // [49,52) base offset (0: atoms are 1024-byte aligned), [61,64) layout (2 = 128B swizzle).
@@ -259,6 +265,31 @@ __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
 
 namespace attn {
 
+// Four fp32 -> four e4m3 codes (OCP FP8: round to nearest even, saturating
+// to +-448), x0 in the lowest byte.
+__device__ __forceinline__ uint32_t pack_e4m3x4(float x0, float x1, float x2, float x3) {
+  uint32_t r;
+  asm("{\n\t.reg .b16 lo, hi;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 lo, %2, %1;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 hi, %4, %3;\n\t"
+      "mov.b32 %0, {lo, hi};\n\t}"
+      : "=r"(r)
+      : "f"(x0), "f"(x1), "f"(x2), "f"(x3));
+  return r;
+}
+// The e4m3 value nearest to x (as pack_e4m3x4 rounds it), back in fp32.
+__device__ __forceinline__ float round_e4m3(float x) {
+  float y;
+  asm("{\n\t.reg .b16 c, lo, hi;\n\t.reg .b32 h2;\n\t"
+      "cvt.rn.satfinite.e4m3x2.f32 c, %1, %1;\n\t"
+      "cvt.rn.f16x2.e4m3x2 h2, c;\n\t"
+      "mov.b32 {lo, hi}, h2;\n\t"
+      "cvt.f32.f16 %0, lo;\n\t}"
+      : "=f"(y)
+      : "f"(x));
+  return y;
+}
+
 // 16-byte shared-memory load/store through 32-bit shared addresses.
 __device__ __forceinline__ float4 lds_f4(uint32_t addr) {
   float4 v;
@@ -322,6 +353,17 @@ __device__ __forceinline__ void mma_ts_warp(uint32_t d_tmem, uint32_t a_tmem, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "@e tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// D(tmem) (+)= A(smem desc) * B(smem desc), 8-bit operands (K = 32 per instruction).
+__device__ __forceinline__ void mma_ss_f8_warp(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p, e;\n\t"
+      "elect.sync _|e, 0xffffffff;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "@e tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 __device__ __forceinline__ void tc_commit_warp(uint32_t bar) {

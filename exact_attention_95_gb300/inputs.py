@@ -160,6 +160,23 @@ def make_tensor(seed: int, shape, dtype: str, mul: float = 1.0,
     return out.reshape(shape)
 
 
+def make_blocky_tensor(seed: int, shape, block: int = 128, exps=(-1, 0, 1)) -> np.ndarray:
+    """bf16 bits of make_tensor(seed, shape) with every `block` rows of each head
+    multiplied by 2^e, e drawn uniformly from `exps` (exact: powers of two).
+
+    Block quantization gives each 128-row block its own scale; varying the
+    magnitude per block makes a wrong block index visible in the output."""
+    base = make_tensor(seed, shape, "bf16")
+    *lead, N, d = shape
+    heads = int(np.prod(lead)) if lead else 1
+    T = -(-N // block)
+    words = splitmix64(seed ^ 0xB10C, 0, heads * T)
+    e = np.asarray(exps, dtype=np.float64)[(words % np.uint64(len(exps))).astype(np.int64)].reshape(heads, T)
+    mul = np.repeat(np.exp2(e), block, axis=1)[:, :N]
+    x = bf16_bits_to_f64(base).reshape(heads, N, d) * mul[:, :, None]
+    return round_to_bf16_bits(x).reshape(shape)
+
+
 def workload_tensors(w: Workload, names=("Q", "K", "V", "dO"), shape_override=None):
     """The seeded tensors of a workload as numpy arrays (bf16 bits or fp32)."""
     out = {}

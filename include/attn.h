@@ -31,7 +31,8 @@
  * reported by attn_last_device_status().
  *
  * Errors: ATTN_ERR_INVALID_ARG for null or misaligned pointers, non-positive
- * sizes, Hq % Hkv != 0, a non-finite scale or an unknown dtype;
+ * sizes, Hq % Hkv != 0, a scale that is not finite and positive, or an
+ * unknown dtype;
  * ATTN_ERR_UNSUPPORTED for combinations the kernels do not implement
  * (d other than 64 or 128, fp32 backward, fp32 input with bf16 output);
  * ATTN_ERR_CUDA when a CUDA runtime call or launch fails.  There is no CPU
@@ -120,6 +121,41 @@ attn_status attn_fwd_split(const void* Q, const void* K, const void* V, void* O,
 attn_status attn_fwd_masked(const void* Q, const void* K, const void* V, void* O, float* LSE,
                             int B, int Hq, int Hkv, int N, int d, float scale, int causal,
                             const uint8_t* block_mask, int mask_heads, attn_dtype out_dtype, void* stream);
+
+/*
+ * FP8 block quantization ("02 FlashAttention" §10: FlashAttention-3's FP8
+ * path; §12.2: one scale per block).  Per head and per block of 128
+ * consecutive rows (the last block may be shorter):
+ *   scale = amax / 448 (fp32 division; 1 for an all-zero block),
+ *   code  = e4m3(x / scale)  (fp32 quotient; OCP e4m3, round to nearest even,
+ *           saturating to +-448).
+ *   X      [BH, N, d] bf16 (device)
+ *   codes  transpose = 0: [BH, N, d] uint8;
+ *          transpose = 1: [BH, d, attn_fp8_vt_stride(N)] uint8, codes[b][c][i]
+ *          = code of X[b][i][c], columns i >= N written as 0
+ *   scales [BH, ceil(N / 128)] fp32
+ *   BH, N >= 1; d in {64, 128}.  All outputs fully overwritten.
+ */
+int attn_fp8_vt_stride(int N); /* N rounded up to 16 (0 for N < 1) */
+attn_status attn_quantize_fp8(const void* X, void* codes, float* scales, long long BH, int N, int d,
+                              int transpose, void* stream);
+
+/*
+ * FP8 forward on block-quantized inputs: the function of attn_fwd evaluated
+ * on the dequantized tensors Q = sq * Qc, K = sk * Kc, V = sv * Vc (the scale
+ * of each element's 128-row block).  Both products run on e4m3 tensor cores
+ * with fp32 accumulation; the probabilities P are rounded to e4m3 before P V
+ * (scaled per key block so that P <= 256), the row sums use the unrounded P.
+ *   Qc [B,Hq,N,128], Kc [B,Hkv,N,128] uint8 codes, q_scale [B,Hq,T],
+ *   k_scale and v_scale [B,Hkv,T] fp32 with T = ceil(N / 128), Vtc the V
+ *   codes transposed, [B,Hkv,128,attn_fp8_vt_stride(N)] (as written by
+ *   attn_quantize_fp8 with transpose = 1); all scales > 0.
+ *   O [B,Hq,N,128] out_dtype (bf16 or fp32), LSE [B,Hq,N] fp32.
+ *   d must be 128 (else ATTN_ERR_UNSUPPORTED).  Other rules as attn_fwd.
+ */
+attn_status attn_fwd_fp8(const void* Qc, const float* q_scale, const void* Kc, const float* k_scale,
+                         const void* Vtc, const float* v_scale, void* O, float* LSE, int B, int Hq, int Hkv,
+                         int N, int d, float scale, int causal, attn_dtype out_dtype, void* stream);
 
 /*
  * Block-sparse backward: attn_bwd with the block mask of attn_fwd_masked

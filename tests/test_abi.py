@@ -182,3 +182,45 @@ def test_masked_argument_errors(lib):
     assert bwd(mh=5) == pkg.ATTN_ERR_INVALID_ARG
     assert bwd(ws=None) == pkg.ATTN_ERR_INVALID_ARG
     assert bwd(Hq=64, Hkv=1, N=128 * 65, mh=1) == pkg.ATTN_ERR_UNSUPPORTED  # 64 x 65 > 4096 pairs
+
+
+def test_fp8_argument_errors(lib):
+    assert lib.attn_fp8_vt_stride(1) == 16 and lib.attn_fp8_vt_stride(4096) == 4096
+    assert lib.attn_fp8_vt_stride(300) == 304 and lib.attn_fp8_vt_stride(0) == 0
+    S = ctypes.c_void_p(0x30000)
+
+    def fwd(**kw):
+        a = dict(Q=A, sq=S, K=A, sk=S, V=A, sv=S, O=A, LSE=A, B=1, Hq=2, Hkv=1, N=256, d=128, scale=0.125,
+                 causal=1, outd=0)
+        a.update(kw)
+        return lib.attn_fwd_fp8(a["Q"], a["sq"], a["K"], a["sk"], a["V"], a["sv"], a["O"], a["LSE"], a["B"],
+                                a["Hq"], a["Hkv"], a["N"], a["d"], a["scale"], a["causal"], a["outd"], None)
+
+    assert fwd(sq=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(sv=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(sk=ctypes.c_void_p(0x30002)) == pkg.ATTN_ERR_INVALID_ARG  # misaligned scales
+    assert fwd(V=ctypes.c_void_p(0x10008)) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(scale=0.0) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(scale=-0.125) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(outd=5) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(Hq=3, Hkv=2) == pkg.ATTN_ERR_INVALID_ARG
+    assert fwd(d=64) == pkg.ATTN_ERR_UNSUPPORTED  # the FP8 kernel is d = 128 only
+
+    def quant(**kw):
+        a = dict(X=A, c=A, s=S, BH=4, N=300, d=128, tr=1)
+        a.update(kw)
+        return lib.attn_quantize_fp8(a["X"], a["c"], a["s"], a["BH"], a["N"], a["d"], a["tr"], None)
+
+    assert quant(X=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(s=None) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(N=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(BH=0) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(tr=2) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(c=ctypes.c_void_p(0x10004)) == pkg.ATTN_ERR_INVALID_ARG
+    assert quant(d=96) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def test_nonpositive_scale_is_rejected(lib):
+    # The kernels take the row max on the unscaled scores: the scale must be > 0.
+    assert _fwd(lib, scale=0.0) == pkg.ATTN_ERR_INVALID_ARG
+    assert _fwd(lib, scale=-1.0) == pkg.ATTN_ERR_INVALID_ARG
