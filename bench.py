@@ -783,7 +783,8 @@ def run_fp8(args, pkg, rank, world, dev):
                  "ms_quantize_qkv": ms_quant,
                  "quantize_hbm_frac": q_bytes / (ms_quant / 1e3) / 1e9 / hbm},
         "roofline": {"bound": "tensor", "achieved": value / world, "peak": fp8_peak, "unit": "TFLOP/s",
-                     "frac": value / world / fp8_peak, "traffic": None, "kernel": "fwd_fp8_kernel",
+                     "frac": value / world / fp8_peak, "traffic": load_traffic("fwd_fp8", "fp8"),
+                     "kernel": "fwd_fp8_kernel",
                      "peak_source": f"2 x bf16_tflops of {peak_src} (nominal fp8:bf16 dense ratio 4.5:2.25)"},
         "e2e": {"value": flops * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
@@ -835,7 +836,12 @@ def load_traffic(kernel_desc, workload):
             d = json.load(f)
     except (OSError, ValueError):
         return None
-    key, src = ("bwd_main", "bwd_sm103.cu") if kernel_desc.startswith("bwd_main") else ("fwd", "fwd_sm103.cu")
+    if kernel_desc.startswith("bwd_main"):
+        key, src = "bwd_main", "bwd_sm103.cu"
+    elif kernel_desc.startswith("fwd_fp8"):
+        key, src = "fwd_fp8", "fp8.cu"
+    else:
+        key, src = "fwd", "fwd_sm103.cu"
     ent = d.get(key)
     if not ent or ent.get("workload") != workload or ent.get("source_sha256") != kernel_source_sha(src):
         return None
