@@ -38,6 +38,7 @@ METRIC = "attention fwd/bwd TFLOPS (bf16, causal, N=4K, d=128) and % of GB300 te
 WORKLOAD = "c3"
 FALLBACK_PEAK = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0, "hbm_gbs": 6800.0}
 L2_BYTES = 126 * 1024 * 1024
+SPARSE_MASK_SEED = 0x5EED0B5
 
 
 def parse_args(argv=None):
@@ -617,7 +618,7 @@ def run_sparse(args, pkg, rank, world, dev):
     Q, K, V, dO = (torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).to(dev)
                    for k in ("Q", "K", "V", "dO"))
     T = (w.N + 127) // 128
-    mask_np = (np.random.default_rng(0x5EED).random((1, T, T)) < 0.5).astype(np.uint8)
+    mask_np = inputs.random_block_mask(SPARSE_MASK_SEED, 1, T, 0.5)
     mask = torch.from_numpy(mask_np).to(dev)
     # Kept scores per head: causal lower triangle restricted to kept blocks.
     idx = np.arange(w.N)
@@ -849,48 +850,102 @@ def load_traffic(kernel_desc, workload):
 
 
 def run_e2e(args, pkg, w, t_np, dev, stream, flops, world):
-    """Same step through the public API with pinned host buffers: H2D of the
-    inputs and D2H of O, dQ, dK, dV inside the timed region."""
+    """The step through the public API from pinned host memory: every step
+    copies its inputs Q, K, V, dO host -> device and its results O, dQ, dK, dV
+    device -> host inside the timed region.
+
+    Measured as a training loop runs it: the next step's inputs are uploaded
+    and the previous step's results downloaded on two copy streams while the
+    current step's kernels run (two device slots, events between the
+    streams).  The same steps run back to back on one stream are reported as
+    `serial_ms_per_step`."""
     import numpy as np
     import torch
 
     host = {k: torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).pin_memory()
             for k in ("Q", "K", "V", "dO")}
-    dbuf = {k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in host.items()}
     out_shapes = {"O": host["Q"].shape, "dQ": host["Q"].shape, "dK": host["K"].shape,
                   "dV": host["V"].shape}
     hout = {k: torch.empty(s, dtype=torch.bfloat16).pin_memory() for k, s in out_shapes.items()}
-    LSE = torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev)
+    slots = 2
+    din = [{k: torch.empty(v.shape, dtype=torch.bfloat16, device=dev) for k, v in host.items()}
+           for _ in range(slots)]
+    dout = [{k: torch.empty(s, dtype=torch.bfloat16, device=dev) for k, s in out_shapes.items()}
+            for _ in range(slots)]
+    lse = [torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev) for _ in range(slots)]
     ws = torch.empty(pkg.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
                      device=dev)
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(slots)]    # slot's inputs uploaded
+    ev_used = [torch.cuda.Event() for _ in range(slots)]  # slot's kernels done
+    ev_out = [torch.cuda.Event() for _ in range(slots)]   # slot's results downloaded
 
-    def step():
-        for k in dbuf:
-            dbuf[k].copy_(host[k], non_blocking=True)
-        O, L = pkg.attn_fwd(dbuf["Q"], dbuf["K"], dbuf["V"], w.scale, w.causal, LSE=LSE,
-                            stream=stream)
-        dQ, dK, dV = pkg.attn_bwd(dbuf["Q"], dbuf["K"], dbuf["V"], O, dbuf["dO"], L, w.scale,
-                                  w.causal, workspace=ws, stream=stream)
-        for k, t in (("O", O), ("dQ", dQ), ("dK", dK), ("dV", dV)):
-            hout[k].copy_(t, non_blocking=True)
+    def compute(a, o, L, st):
+        pkg.attn_fwd(a["Q"], a["K"], a["V"], w.scale, w.causal, O=o["O"], LSE=L, stream=st)
+        pkg.attn_bwd(a["Q"], a["K"], a["V"], o["O"], a["dO"], L, w.scale, w.causal, o["dQ"], o["dK"],
+                     o["dV"], workspace=ws, stream=st)
 
-    for _ in range(2):
-        step()
-    torch.cuda.synchronize()
+    def pipelined(i):
+        s = i % slots
+        if i >= slots:
+            s_in.wait_event(ev_used[s])
+        with torch.cuda.stream(s_in):
+            for k in host:
+                din[s][k].copy_(host[k], non_blocking=True)
+        ev_in[s].record(s_in)
+        stream.wait_event(ev_in[s])
+        if i >= slots:
+            stream.wait_event(ev_out[s])
+        compute(din[s], dout[s], lse[s], stream)
+        ev_used[s].record(stream)
+        s_out.wait_event(ev_used[s])
+        with torch.cuda.stream(s_out):
+            for k in hout:
+                hout[k].copy_(dout[s][k], non_blocking=True)
+        ev_out[s].record(s_out)
+
+    def serial():
+        for k in host:
+            din[0][k].copy_(host[k], non_blocking=True)
+        compute(din[0], dout[0], lse[0], stream)
+        for k in hout:
+            hout[k].copy_(dout[0][k], non_blocking=True)
+
     n = max(1, args.e2e_steps)
+    for i in range(slots):
+        pipelined(i)
+    serial()
+    torch.cuda.synchronize()
+    if pkg.attn_last_device_status() != pkg.ATTN_OK:
+        raise RuntimeError("device status not OK in the e2e warm-up")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
-    for _ in range(n):
-        step()
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(n):
+        pipelined(i)
+    stream.wait_event(ev_out[(n - 1) % slots])
     e1.record(stream)
     torch.cuda.synchronize()
     ms = max_over_ranks(e0.elapsed_time(e1), dev) / n
+    e0.record(stream)
+    for _ in range(n):
+        serial()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    ms_serial = max_over_ranks(e0.elapsed_time(e1), dev) / n
+    if pkg.attn_last_device_status() != pkg.ATTN_OK:
+        raise RuntimeError("device status not OK in the e2e region")
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = sum(t.numel() * t.element_size() for t in hout.values())
     return {"value": flops * world / (ms / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms,
-            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "overlap": "step i+1's uploads and step i-1's downloads run on two copy streams "
+                       "beside step i's kernels (two device slots)",
+            "serial_ms_per_step": ms_serial,
+            "serial_tflops": flops * world / (ms_serial / 1e3) / 1e12}
 
 
 def cpu_baseline(w, budget_s):

@@ -177,6 +177,13 @@ def make_blocky_tensor(seed: int, shape, block: int = 128, exps=(-1, 0, 1)) -> n
     return round_to_bf16_bits(x).reshape(shape)
 
 
+def random_block_mask(seed: int, heads: int, T: int, density: float) -> np.ndarray:
+    """uint8 [heads, T, T] block mask, each entry kept with probability `density`
+    (uniforms from the SplitMix64 stream of `seed`)."""
+    u = (splitmix64(seed, 0, heads * T * T) >> np.uint64(11)).astype(np.float64) * (2.0 ** -53)
+    return (u < density).astype(np.uint8).reshape(heads, T, T)
+
+
 def workload_tensors(w: Workload, names=("Q", "K", "V", "dO"), shape_override=None):
     """The seeded tensors of a workload as numpy arrays (bf16 bits or fp32)."""
     out = {}

@@ -90,3 +90,35 @@ def test_all_ones_mask_equals_dense():
         gm = pkg.attn_bwd_masked(g["Q"], g["K"], g["V"], Od, g["dO"], Ld, ones, None, causal)
         for a, b in zip(gd, gm):
             assert (a.float() - b.float()).abs().max().item() <= 2e-2 * a.float().abs().max().item()
+
+
+def test_blocksparse_bench_workload_two_heads():
+    """The block-sparse benchmark's launch: the c3 tensors (B2 H32 N4096 d128,
+    causal, Q x8) with its density-1/2 mask shared by all heads; forward with
+    bf16 O and the backward reading it.  Two whole heads against the oracle."""
+    import bench
+    w = inputs.WORKLOADS["c3"]
+    t = inputs.workload_tensors(w)
+    g = {k: to_dev(v) for k, v in t.items()}
+    T = (w.N + 127) // 128
+    m = inputs.random_block_mask(bench.SPARSE_MASK_SEED, 1, T, 0.5)
+    gm = torch.from_numpy(m).cuda()
+    O, L = pkg.attn_fwd_masked(g["Q"], g["K"], g["V"], gm, w.scale, w.causal)
+    dQ, dK, dV = pkg.attn_bwd_masked(g["Q"], g["K"], g["V"], O, g["dO"], L, gm, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert pkg.attn_last_device_status() == pkg.ATTN_OK
+    for b, h in ((0, 0), (1, 31)):
+        f = {k: inputs.to_f64(v[b:b + 1, h:h + 1]) for k, v in t.items()}
+        ref = oracle.bwd_masked(f["Q"], f["K"], f["V"], f["dO"], w.scale, w.causal, m)
+        Og, Lg = f64(O[b:b + 1, h:h + 1]), f64(L[b:b + 1, h:h + 1])
+        empty = np.isneginf(ref["LSE"])
+        assert np.array_equal(np.isneginf(Lg), empty)
+        err_o, ok = check_o(Og, ref["O"], bf16_out=True)
+        assert ok, f"head ({b},{h}) O max-abs {err_o:.3e}"
+        assert np.abs(Lg[~empty] - ref["LSE"][~empty]).max() <= LSE_TOL
+        # The oracle's gradients use its own O; the GPU's use its bf16 O (as a
+        # training step does): both within the gradient tolerance.
+        for name, got in (("dQ", dQ), ("dK", dK), ("dV", dV)):
+            e = rel_err(f64(got[b:b + 1, h:h + 1]), ref[name])
+            assert e <= GRAD_TOL, f"head ({b},{h}) {name} rel err {e:.3e}"
+    assert torch.isfinite(dQ).all() and torch.isfinite(dK).all() and torch.isfinite(dV).all()

@@ -86,24 +86,29 @@ def _fp8_inputs(B, Hq, Hkv, N, seed, exps=(-1, 0, 1)):
     return dev, host
 
 
+def _o_bound_rows(q, k, v, sv, scale, causal, rows, oref):
+    """Bound for query rows `rows` of one head: q [R, d] those rows, k, v [N, d],
+    sv [T] the head's V block scales, oref [R, d] the reference rows."""
+    N = k.shape[0]
+    keep = (np.arange(N)[None, :] <= np.asarray(rows)[:, None]) if causal else np.ones((len(rows), N), dtype=bool)
+    s = np.where(keep, scale * (q @ k.T), -np.inf)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    rinv = np.repeat(sv.max() / sv, 128)[:N]
+    e = np.where(keep, np.maximum(2.0 ** -4 * w, np.minimum(w, 2.0 ** -14 * rinv[None, :])), 0.0)
+    den = w.sum(axis=1, keepdims=True)
+    return 1.25 * (e @ np.abs(v) + np.abs(oref) * e.sum(axis=1, keepdims=True)) / den + 1e-5
+
+
 def _o_bound(Qd, Kd, Vd, sV, scale, causal, Oref):
     """Per-element bound on |O - O_ref| from the e4m3 rounding of P (see above)."""
     B, Hq, N, d = Qd.shape
     G = Hq // Kd.shape[1]
     bound = np.zeros_like(Oref)
-    keep = np.tril(np.ones((N, N), dtype=bool)) if causal else np.ones((N, N), dtype=bool)
     for b in range(B):
         for h in range(Hq):
-            hk = h // G
-            s = scale * (Qd[b, h] @ Kd[b, hk].T)
-            s = np.where(keep, s, -np.inf)
-            w = np.exp(s - s.max(axis=1, keepdims=True))
-            rinv = np.repeat(sV[b, hk].max() / sV[b, hk], 128)[:N]
-            e = np.maximum(2.0 ** -4 * w, np.minimum(w, 2.0 ** -14 * rinv[None, :]))
-            e = np.where(keep, e, 0.0)
-            den = w.sum(axis=1, keepdims=True)
-            bound[b, h] = (e @ np.abs(Vd[b, hk]) + np.abs(Oref[b, h]) * e.sum(axis=1, keepdims=True)) / den
-    return 1.25 * bound + 1e-5
+            bound[b, h] = _o_bound_rows(Qd[b, h], Kd[b, h // G], Vd[b, h // G], sV[b, h // G], scale, causal,
+                                        np.arange(N), Oref[b, h])
+    return bound
 
 
 FWD_CASES = [
@@ -166,3 +171,44 @@ def test_fwd_fp8_equals_quantizer_roundtrip():
                          tensors["V"][1], None, True)
     torch.cuda.synchronize()
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_fwd_fp8_bench_workload_sampled_rows():
+    """The FP8 benchmark's launch: the c3 tensors (B2 H32 N4096 d128, causal,
+    Q x8) quantized by the library, bf16 O.  Checked on 128 seeded rows of each
+    of four heads; the codes of those heads are also compared with the
+    reference quantizer's."""
+    w = inputs.WORKLOADS["c3"]
+    t = inputs.workload_tensors(w, names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    qc, qs = pkg.attn_quantize_fp8(g["Q"])
+    kc, ks = pkg.attn_quantize_fp8(g["K"])
+    vc, vs = pkg.attn_quantize_fp8(g["V"], transpose=True)
+    O, L = pkg.attn_fwd_fp8(qc, qs, kc, ks, vc, vs, w.scale, w.causal)
+    torch.cuda.synchronize()
+    assert pkg.attn_last_device_status() == pkg.ATTN_OK
+    assert torch.isfinite(O).all() and torch.isfinite(L).all()
+    dev_codes = {"Q": (qc, qs), "K": (kc, ks), "V": (vc, vs)}
+    for b, h in ((0, 0), (0, 13), (1, 7), (1, 31)):
+        deq, sv = {}, None
+        for name in ("Q", "K", "V"):
+            tr = name == "V"
+            x = _bits_to_f32(t[name][b, h])[None]
+            c, s = ofp8.quantize_blocks(x, transpose=tr)
+            dc, ds = dev_codes[name]
+            assert np.array_equal(dc[b, h].cpu().numpy(), c[0]), f"{name} codes of head ({b},{h})"
+            assert np.array_equal(ds[b, h].cpu().numpy(), s[0])
+            deq[name] = ofp8.dequantize_blocks(c, s, transpose=tr)[0]
+            if tr:
+                sv = s[0].astype(np.float64)
+        rows = inputs.sample_rows(0xF8C3 + 64 * b + h, w.N, 128, must=[0, 1, 127, 128, w.N - 1])
+        Oref, Lref = oracle.fwd_rows(deq["Q"][None, None], deq["K"][None, None], deq["V"][None, None], w.scale,
+                                     w.causal, rows)
+        Oref = Oref.reshape(len(rows), w.d)
+        Lref = Lref.reshape(len(rows))
+        bound = _o_bound_rows(deq["Q"][rows], deq["K"], deq["V"], sv, w.scale, w.causal, rows, Oref)
+        half_ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(Oref), 2.0 ** -126))) - 8)
+        Og = f64(O[b, h])[rows]
+        err = np.abs(Og - Oref)
+        assert np.all(err <= bound + half_ulp), f"head ({b},{h}): {float((err - bound - half_ulp).max()):.3e}"
+        assert np.abs(f64(L[b, h])[rows] - Lref).max() <= LSE_TOL
