@@ -149,25 +149,41 @@ namespace {
 
 constexpr int kMaxSplits = 256;
 
-// Number of key splits: the caller's, or (num_splits == 0) enough to give the
-// forward about two CTAs per SM, at most one split per 128-key tile.  The
-// result never leaves a split without a tile.  -1 for an invalid request.
+// Number of key splits: the caller's, or (num_splits == 0) one when the
+// unsplit grid already fills the SMs, else the count that minimises the
+// forward's span with one CTA per SM: waves (ceil of CTAs / SMs) times (tiles
+// per split + one tile's worth of per-CTA prologue and epilogue), preferring
+// fewer splits on ties; at most 64 and one split per 128-key tile.  The result
+// never leaves a split without a tile.  -1 for an invalid request.
 int fwd_splits(int B, int Hq, int Hkv, int Nq, int Nk, int num_splits) {
   if (num_splits < 0 || num_splits > kMaxSplits) return -1;
   const int ktiles = (Nk + 127) / 128;
-  int want = num_splits;
-  if (want == 0) {
-    int dev = 0, sms = 148;
-    cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    const int G = Hq / Hkv;
-    const bool packed = G > 1 && (long long)G * Nq <= 128;  // as in fwd_bf16_run
-    const long long ctas = packed ? (long long)B * Hkv : (long long)B * Hq * (((Nq + 127) / 128 + 1) / 2);
-    want = (int)std::min<long long>(64, std::max<long long>(1, (2LL * sms + ctas - 1) / ctas));
+  auto rounded = [&](int want) {
+    want = std::max(1, std::min(want, ktiles));
+    const int per = (ktiles + want - 1) / want;
+    return (ktiles + per - 1) / per;
+  };
+  if (num_splits > 0) return rounded(num_splits);
+  int dev = 0, sms = 148;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int G = Hq / Hkv;
+  const bool packed = G > 1 && (long long)G * Nq <= 128;  // as in fwd_bf16_run
+  const long long ctas = packed ? (long long)B * Hkv : (long long)B * Hq * (((Nq + 127) / 128 + 1) / 2);
+  if (ctas >= sms) return 1;
+  int best = 1;
+  long long best_cost = -1;
+  for (int want = 1; want <= std::min(64, ktiles); ++want) {
+    const int s = rounded(want);
+    const long long per = (ktiles + s - 1) / s;
+    const long long waves = (ctas * s + sms - 1) / sms;
+    const long long cost = waves * (per + 1);
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
   }
-  want = std::min(want, ktiles);
-  const int per = (ktiles + want - 1) / want;
-  return (ktiles + per - 1) / per;
+  return best;
 }
 
 size_t fwd_split_lse_offset(long long rows, int d, int splits) {

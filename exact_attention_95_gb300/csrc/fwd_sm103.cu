@@ -53,14 +53,17 @@ static_assert(128 * kRegsLow + 256 * kRegsHigh <= kThreads * kLaunchRegs,
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleThreshold = 16.0f;  // log2 units: rescale when m grows by > 2^16
 
-template <int D>
+// ONE: the one-query-tile variant holds one Q tile and gives the space to
+// the K/V ring (it streams K and V for few rows: decoding).
+template <int D, bool ONE = false>
 struct Fwd {
   static constexpr int CB = D / 64;              // 128-byte column blocks per row
   static constexpr int BLOCK_BYTES = 128 * 128;  // one 128-row x 64-col bf16 block
   static constexpr int TILE_BYTES = CB * BLOCK_BYTES;
-  static constexpr int STAGES = D == 128 ? 4 : 8;
-  static constexpr int OFF_Q = 0;                // two Q tiles
-  static constexpr int OFF_KV = 2 * TILE_BYTES;
+  static constexpr int QT = ONE ? 1 : 2;         // Q tiles held
+  static constexpr int STAGES = (D == 128 ? 4 : 8) + (ONE ? 1 : 0);  // a stage = one tile
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_KV = QT * TILE_BYTES;
   static constexpr int OFF_BAR = OFF_KV + STAGES * TILE_BYTES;
   static constexpr int B_QFULL = 0;
   static constexpr int B_KVFULL = 1;
@@ -76,6 +79,7 @@ struct Fwd {
   static constexpr int OFF_NLIST = OFF_ABORT + 4;           // block-sparse: entries in the tile list
   static constexpr int OFF_LIST = OFF_NLIST + 4;            // uint16 per listed K/V tile
   static constexpr int SMEM_BYTES = OFF_LIST + 2 * kMaxMaskTiles + 1024;  // + alignment slack
+  static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per block");
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t IDESC_O = idesc_bf16(kBM, D, false, true);
   static constexpr uint32_t TM_S = 0;    // one S buffer shared by both tiles (128 columns)
@@ -90,7 +94,7 @@ template <int D, bool ONE, bool MASKED>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_bf16_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const FwdParams p) {
-  using C = Fwd<D>;
+  using C = Fwd<D, ONE>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
@@ -193,8 +197,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmQ);
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
-      mbar_arrive_expect_tx(bar(C::B_QFULL), 2 * C::TILE_BYTES);
-      for (int t = 0; t < 2; ++t)
+      mbar_arrive_expect_tx(bar(C::B_QFULL), C::QT * C::TILE_BYTES);
+      for (int t = 0; t < C::QT; ++t)
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(sQ + t * C::TILE_BYTES + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64,
                       q0 + t * kBM, bh);
@@ -515,7 +519,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int D, bool ONE, bool MASKED>
 cudaError_t launch_one(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                        const FwdParams& p, cudaStream_t stream) {
-  using C = Fwd<D>;
+  using C = Fwd<D, ONE>;
   auto kern = fwd_bf16_kernel<D, ONE, MASKED>;
   // setmaxnreg moves registers inside the launch allocation; refuse to launch
   // if the compiler gave the kernel a different per-thread count than assumed

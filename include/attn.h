@@ -95,7 +95,9 @@ attn_status attn_fwd(const void* Q, const void* K, const void* V, void* O, float
  *   O [B,Hq,Nq,d]                        out_dtype: bf16 or fp32
  *   LSE [B,Hq,Nq] fp32
  *   B, Hq, Hkv, Nq, Nk >= 1; Hq % Hkv == 0; d in {64, 128}; causal in {0, 1}.
- *   num_splits: 0 chooses (about two CTAs per SM), else 1..256; it is capped
+ *   num_splits: 0 chooses (1 when the unsplit grid fills the GPU, else the
+ *     count that completes in the fewest waves of one CTA per SM), else
+ *     1..256; it is capped
  *     at one split per 128-key tile and rounded so that no split is empty.
  *   workspace: attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)
  *     bytes, 256-byte aligned, owned by the caller, not shared with a
