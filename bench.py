@@ -758,19 +758,30 @@ def run_fp8(args, pkg, rank, world, dev):
     q_bytes = 3 * elems + 4 * sum(t.numel() for t in (qs, ks, vs)) + (vc.numel() - V.numel())
     hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAK["hbm_gbs"]))
 
-    # e2e: pinned host bf16 inputs -> device, quantize, forward, O back to the host.
+    # e2e: pinned host bf16 inputs -> device, quantize, forward, O back to the
+    # host; the next step's upload and the previous step's download overlap
+    # the current step's kernels (two device slots).
     host = {k: torch.from_numpy(t_np[k].view(np.int16)).view(torch.bfloat16).pin_memory() for k in ("Q", "K", "V")}
     hout = torch.empty(O.shape, dtype=torch.bfloat16).pin_memory()
+    slot_in = [dict(Q=Q, K=K, V=V)] + [{k: torch.empty_like(v) for k, v in dict(Q=Q, K=K, V=V).items()}]
+    slot_q = [(qc, qs, kc, ks, vc, vs)] + [tuple(torch.empty_like(x) for x in (qc, qs, kc, ks, vc, vs))]
+    slot_o = [O, torch.empty_like(O)]
 
-    def e2e_step():
-        Q.copy_(host["Q"], non_blocking=True)
-        K.copy_(host["K"], non_blocking=True)
-        V.copy_(host["V"], non_blocking=True)
-        quant_step()
-        fp8_step()
-        hout.copy_(O, non_blocking=True)
+    def e2e_upload(sl, st):
+        for k in host:
+            slot_in[sl][k].copy_(host[k], non_blocking=True)
 
-    ms_e2e = timed(e2e_step, max(1, args.e2e_steps))
+    def e2e_compute(sl, st):
+        a, (q_c, q_s, k_c, k_s, v_c, v_s) = slot_in[sl], slot_q[sl]
+        pkg.attn_quantize_fp8(a["Q"], codes=q_c, scales=q_s, stream=st)
+        pkg.attn_quantize_fp8(a["K"], codes=k_c, scales=k_s, stream=st)
+        pkg.attn_quantize_fp8(a["V"], transpose=True, codes=v_c, scales=v_s, stream=st)
+        pkg.attn_fwd_fp8(q_c, q_s, k_c, k_s, v_c, v_s, w.scale, w.causal, O=slot_o[sl], LSE=L, stream=st)
+
+    def e2e_download(sl, st):
+        hout.copy_(slot_o[sl], non_blocking=True)
+
+    ms_e2e = time_pipelined(max(1, args.e2e_steps), e2e_upload, e2e_compute, e2e_download, stream, dev)
     line = {
         "metric": "attention fwd TFLOPS (fp8 e4m3 with per-block scales, causal, N=4K, d=128)",
         "value": value, "unit": "TFLOPS", "n_gpus": world, "steps": args.steps,
@@ -789,7 +800,9 @@ def run_fp8(args, pkg, rank, world, dev):
                      "peak_source": f"2 x bf16_tflops of {peak_src} (nominal fp8:bf16 dense ratio 4.5:2.25)"},
         "e2e": {"value": flops * world / (ms_e2e / 1e3) / 1e12, "unit": "TFLOPS", "ms_per_step": ms_e2e,
                 "h2d_bytes_per_step": sum(t.numel() * t.element_size() for t in host.values()),
-                "d2h_bytes_per_step": hout.numel() * hout.element_size()},
+                "d2h_bytes_per_step": hout.numel() * hout.element_size(),
+                "overlap": "step i+1's upload and step i-1's download run on two copy streams beside "
+                           "step i's quantization and forward (two device slots)"},
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
@@ -849,6 +862,53 @@ def load_traffic(kernel_desc, workload):
     return ent.get("bytes_per_launch")
 
 
+def time_pipelined(n, upload, compute, download, stream, dev, slots=2):
+    """Milliseconds per step of n steps where step i's upload (host -> device
+    slot i % slots), compute and download (slot -> host) run on three streams:
+    uploads wait until the slot's previous compute is done, compute waits for
+    its upload and for the slot's previous download, downloads wait for their
+    compute.  Two warm-up steps run first."""
+    import torch
+
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(slots)]
+    ev_used = [torch.cuda.Event() for _ in range(slots)]
+    ev_out = [torch.cuda.Event() for _ in range(slots)]
+
+    def step(i):
+        sl = i % slots
+        if i >= slots:
+            s_in.wait_event(ev_used[sl])
+        with torch.cuda.stream(s_in):
+            upload(sl, s_in)
+        ev_in[sl].record(s_in)
+        stream.wait_event(ev_in[sl])
+        if i >= slots:
+            stream.wait_event(ev_out[sl])
+        compute(sl, stream)
+        ev_used[sl].record(stream)
+        s_out.wait_event(ev_used[sl])
+        with torch.cuda.stream(s_out):
+            download(sl, s_out)
+        ev_out[sl].record(s_out)
+
+    for i in range(slots):
+        step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    s_in.wait_event(e0)
+    s_out.wait_event(e0)
+    for i in range(n):
+        step(i)
+    stream.wait_event(ev_out[(n - 1) % slots])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return max_over_ranks(e0.elapsed_time(e1), dev) / n
+
+
 def run_e2e(args, pkg, w, t_np, dev, stream, flops, world):
     """The step through the public API from pinned host memory: every step
     copies its inputs Q, K, V, dO host -> device and its results O, dQ, dK, dV
@@ -875,34 +935,19 @@ def run_e2e(args, pkg, w, t_np, dev, stream, flops, world):
     lse = [torch.empty(w.B, w.Hq, w.N, dtype=torch.float32, device=dev) for _ in range(slots)]
     ws = torch.empty(pkg.attn_bwd_workspace_size(w.B, w.Hq, w.Hkv, w.N, w.d), dtype=torch.uint8,
                      device=dev)
-    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    ev_in = [torch.cuda.Event() for _ in range(slots)]    # slot's inputs uploaded
-    ev_used = [torch.cuda.Event() for _ in range(slots)]  # slot's kernels done
-    ev_out = [torch.cuda.Event() for _ in range(slots)]   # slot's results downloaded
 
     def compute(a, o, L, st):
         pkg.attn_fwd(a["Q"], a["K"], a["V"], w.scale, w.causal, O=o["O"], LSE=L, stream=st)
         pkg.attn_bwd(a["Q"], a["K"], a["V"], o["O"], a["dO"], L, w.scale, w.causal, o["dQ"], o["dK"],
                      o["dV"], workspace=ws, stream=st)
 
-    def pipelined(i):
-        s = i % slots
-        if i >= slots:
-            s_in.wait_event(ev_used[s])
-        with torch.cuda.stream(s_in):
-            for k in host:
-                din[s][k].copy_(host[k], non_blocking=True)
-        ev_in[s].record(s_in)
-        stream.wait_event(ev_in[s])
-        if i >= slots:
-            stream.wait_event(ev_out[s])
-        compute(din[s], dout[s], lse[s], stream)
-        ev_used[s].record(stream)
-        s_out.wait_event(ev_used[s])
-        with torch.cuda.stream(s_out):
-            for k in hout:
-                hout[k].copy_(dout[s][k], non_blocking=True)
-        ev_out[s].record(s_out)
+    def upload(sl, st):
+        for k in host:
+            din[sl][k].copy_(host[k], non_blocking=True)
+
+    def download(sl, st):
+        for k in hout:
+            hout[k].copy_(dout[sl][k], non_blocking=True)
 
     def serial():
         for k in host:
@@ -912,24 +957,11 @@ def run_e2e(args, pkg, w, t_np, dev, stream, flops, world):
             hout[k].copy_(dout[0][k], non_blocking=True)
 
     n = max(1, args.e2e_steps)
-    for i in range(slots):
-        pipelined(i)
+    ms = time_pipelined(n, upload, lambda sl, st: compute(din[sl], dout[sl], lse[sl], st), download, stream, dev,
+                        slots)
     serial()
     torch.cuda.synchronize()
-    if pkg.attn_last_device_status() != pkg.ATTN_OK:
-        raise RuntimeError("device status not OK in the e2e warm-up")
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier()
-    torch.cuda.synchronize()
-    e0.record(stream)
-    s_in.wait_event(e0)
-    s_out.wait_event(e0)
-    for i in range(n):
-        pipelined(i)
-    stream.wait_event(ev_out[(n - 1) % slots])
-    e1.record(stream)
-    torch.cuda.synchronize()
-    ms = max_over_ranks(e0.elapsed_time(e1), dev) / n
     e0.record(stream)
     for _ in range(n):
         serial()

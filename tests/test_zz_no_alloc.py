@@ -65,6 +65,6 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert pkg.attn_bwd_workspace_size(B, Hq, Hkv, N, d) > pkg.NOALLOC_SCRATCH_BYTES
     rc = fn(A, A, A, A, A, A, A, A, A, B, Hq, Hkv, N, d, 0.1, 1, pkg.ATTN_BF16, None)
     assert rc == pkg.ATTN_ERR_UNSUPPORTED
-    # Invalid sizes still get attn_bwd's own verdicts.
+    # Invalid sizes still get attn_bwd's own error codes.
     assert fn(A, A, A, A, A, A, A, A, A, 1, 3, 2, 64, 128, 0.1, 1, 0, None) == pkg.ATTN_ERR_INVALID_ARG
     assert fn(A, A, A, A, A, A, A, A, A, 1, 2, 2, 64, 96, 0.1, 1, 0, None) == pkg.ATTN_ERR_UNSUPPORTED
