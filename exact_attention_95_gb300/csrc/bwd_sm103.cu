@@ -59,8 +59,14 @@ static_assert(128 * kRegsLow + 256 * kRegsHigh <= kMainThreads * kLaunchRegs,
               "register split exceeds the launch allocation");
 constexpr uint32_t kTmemCols = 512;
 
-template <int D>
+// MASKED: the block-sparse variant, which keeps a list of (query head, query
+// tile) pairs in shared memory.  The dense variant uses that space for a
+// dedicated staging buffer of one dQ half (64 query rows), so that a
+// stage's Q slot is released as soon as dK has read it and only the dO slot
+// waits for a reduce.
+template <int D, bool MASKED>
 struct Bwd {
+  static constexpr bool STAGED = !MASKED;
   static constexpr int CB = D / 64;
   static constexpr int BLK = 128 * 128;  // 128 rows x 128 bytes
   static constexpr int OFF_K = 0;
@@ -73,7 +79,9 @@ struct Bwd {
   static constexpr int ST_D = ST_LSE + kBQ * 4;
   static constexpr int STAGE_BYTES = (ST_D + kBQ * 4 + 1023) / 1024 * 1024;
   static constexpr int STAGES = 2;
-  static constexpr int OFF_BAR = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int DQS_BYTES = 64 * D * 4;  // one staged dQ half: 64 query rows x d fp32
+  static constexpr int OFF_DQS = OFF_STAGE + STAGES * STAGE_BYTES;
+  static constexpr int OFF_BAR = OFF_DQS + (STAGED ? DQS_BYTES : 0);
   static constexpr int B_KVFULL = 0;
   // Each stage has two halves with their own barriers: the Q part (Q tile,
   // -LSE2, -D) and the dO part, released separately by the dQ reducer.
@@ -91,13 +99,16 @@ struct Bwd {
   static constexpr int B_DQFULL = B_KVDONE + 1;
   static constexpr int B_DQFREE = B_DQFULL + 1;
   static constexpr int B_DQSTAGED = B_DQFREE + 1;  // 2: one per math warpgroup
-  static constexpr int B_DRAIN = B_DQSTAGED + 2;
+  static constexpr int B_DQSFREE = B_DQSTAGED + 2; // dense: the staging buffer has been read
+  static constexpr int B_DRAIN = B_DQSFREE + 1;
   static constexpr int NBARS = B_DRAIN + 1;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_NLIST = OFF_ABORT + 4;   // block-sparse: entries in the list
   static constexpr int OFF_LIST = OFF_NLIST + 4;    // uint32 (g << 16 | query tile) per entry
-  static constexpr int SMEM_BYTES = OFF_LIST + 4 * kMaxMaskIters + 1024;
+  // The dense variant has no room for alignment slack: the kernel checks that
+  // the dynamic shared memory starts on a 1024-byte boundary.
+  static constexpr int SMEM_BYTES = MASKED ? OFF_LIST + 4 * kMaxMaskIters + 1024 : OFF_ABORT + 4;
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per block");
   // TMEM columns
   static constexpr uint32_t TM_DV = 0;
@@ -235,13 +246,19 @@ __device__ __forceinline__ void bwd_probs(const uint32_t (&sr)[2][32], uint32_t 
   }
 }
 
-template <int D>
+constexpr int kDevSmemAlign = 2;  // status: dynamic shared memory not 1024-byte aligned
+
+template <int D, bool MASKED>
 __global__ void __launch_bounds__(kMainThreads, 1)
     bwd_main_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmdO,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
-  using C = Bwd<D>;
+  using C = Bwd<D, MASKED>;
   extern __shared__ uint8_t smem_raw[];
+  if (!MASKED && (smem_u32(smem_raw) & 1023u) != 0) {
+    if (threadIdx.x == 0) atomicCAS(p.status, 0, kDevSmemAlign);
+    return;
+  }
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   const uint32_t sb = smem_u32(smem);
@@ -268,7 +285,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   int T = G * per_head;  // inner iterations (>= 1 since k0 < N; may be 0 when masked)
   // Block-sparse: the (query head g, query tile) pairs whose block with this
   // key tile is kept, listed by the otherwise idle warp 3 (ballot compaction).
-  const bool masked = p.bmask != nullptr;
+  constexpr bool masked = MASKED;  // p.bmask != NULL
   uint32_t* const tlist = reinterpret_cast<uint32_t*>(smem + C::OFF_LIST);
   int* const nlist = reinterpret_cast<int*>(smem + C::OFF_NLIST);
   if (masked && warp == 3) {
@@ -304,7 +321,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_STFULL + s), 1);
       mbar_init(bar(C::B_STFULL_DO + s), 1);
-      mbar_init(bar(C::B_STEMPTY + s), 1);     // arrived by the dQ reducer
+      mbar_init(bar(C::B_STEMPTY + s), 1);     // the dQ reducer (dense: committed after dK)
       mbar_init(bar(C::B_STEMPTY_DO + s), 1);  // arrived by the dQ reducer
     }
     mbar_init(bar(C::B_SFULL), 1);
@@ -318,6 +335,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
     mbar_init(bar(C::B_DQFREE), 256);
     mbar_init(bar(C::B_DQSTAGED + 0), 128);
     mbar_init(bar(C::B_DQSTAGED + 1), 128);
+    mbar_init(bar(C::B_DQSFREE), 1);
     mbar_init(bar(C::B_DRAIN), 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -434,6 +452,10 @@ __global__ void __launch_bounds__(kMainThreads, 1)
                       sdesc_sw128(qs + kk * 2048, C::BLK, 1024), C::IDESC_KV,
                       (t > 0 || kk > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_KVDONE));
+        // Dense: dK is the last reader of the stage's Q part (Q, -LSE2, -D; the
+        // math warps read -LSE2 and -D before dS reached TMEM), so the
+        // producer may refill it once dK completes.
+        if (C::STAGED) tc_commit_warp(bar(C::B_STEMPTY + s));
         if (!mbar_wait_warp(bar(C::B_DSSMEM), t & 1, wc)) break;
         tc_fence_after();
         // dQ^T = K^T dS^T: A = K as MN-major [d x keys], B = dS^T in the dO
@@ -458,14 +480,29 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         tile_of(t, g, it);
         const int bhq = b * p.Hq + hk * G + g;
         const uint32_t st = stage(s);
+        const int row0 = (int)((size_t)bhq * p.Npad + (size_t)it * kBQ);
+        if (C::STAGED) {
+          // The half in the dO slot first (the next loads wait for it), then
+          // the half in the staging buffer.
+          if (!mbar_wait(bar(C::B_DQSTAGED + 1), t & 1, wc)) break;
+          tma_reduce_add_2d(&tmDQ, st + C::ST_DO, 0, row0 + 64);
+          bulk_commit_group();
+          if (!mbar_wait(bar(C::B_DQSTAGED + 0), t & 1, wc)) break;
+          tma_reduce_add_2d(&tmDQ, sb + C::OFF_DQS, 0, row0);
+          bulk_commit_group();
+          bulk_wait_read1();
+          mbar_arrive(bar(C::B_STEMPTY_DO + s));
+          bulk_wait_read0();
+          mbar_arrive(bar(C::B_DQSFREE));
+          continue;
+        }
         bool ok = true;
         for (int h = 0; h < 2 && ok; ++h) {
           if (!mbar_wait(bar(C::B_DQSTAGED + h), t & 1, wc)) {
             ok = false;
             break;
           }
-          tma_reduce_add_2d(&tmDQ, st + (h == 0 ? C::ST_Q : C::ST_DO), 0,
-                            (int)((size_t)bhq * p.Npad + (size_t)it * kBQ + 64 * h));
+          tma_reduce_add_2d(&tmDQ, st + (h == 0 ? C::ST_Q : C::ST_DO), 0, row0 + 64 * h);
           bulk_commit_group();
         }
         if (!ok) break;
@@ -579,10 +616,15 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tc_fence_before();
       mbar_arrive(bar(C::B_DQFREE));
       // Stage this half of dQ (64 query rows x d, fp32, row-major) in shared
-      // memory -- warpgroup 0 over the Q slot, warpgroup 1 over the dO slot,
-      // both free once dQ^T has completed -- and add it to the accumulator
-      // with one bulk tensor reduce.
-      const uint32_t qstage = st + (h == 0 ? C::ST_Q : C::ST_DO);
+      // memory -- warpgroup 1 over the dO slot (free once dQ^T has completed),
+      // warpgroup 0 over the staging buffer once the previous tile's reduce
+      // has read it (the masked variant: over the Q slot) -- and add it to
+      // the accumulator with one bulk tensor reduce.
+      const uint32_t qstage = h == 1 ? st + C::ST_DO : C::STAGED ? sb + C::OFF_DQS : st + C::ST_Q;
+      if (C::STAGED && h == 0 && t > 0 && !mbar_wait(bar(C::B_DQSFREE), (t - 1) & 1, wc)) {
+        ok = false;
+        break;
+      }
       if (dcol < D) {
 #pragma unroll
         for (int c = 0; c < 64; ++c) sts_f32(qstage + (c * D + dcol) * 4, __uint_as_float(qr[c >> 5][c & 31]));
@@ -638,11 +680,33 @@ __global__ void __launch_bounds__(kMainThreads, 1)
   }
 }
 
+template <int D, bool MASKED>
+cudaError_t launch_main(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                        const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p,
+                        cudaStream_t stream) {
+  using C = Bwd<D, MASKED>;
+  auto kern = bwd_main_kernel<D, MASKED>;
+  // setmaxnreg moves registers inside the launch allocation; refuse to launch
+  // if the compiler gave the kernel a different per-thread count than assumed.
+  static int regs = -1;  // one per instantiation
+  cudaError_t e;
+  if (regs < 0) {
+    cudaFuncAttributes fa;
+    if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
+    regs = fa.numRegs;
+  }
+  if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+  if (e != cudaSuccess) return e;
+  dim3 grid(p.B * p.Hkv * ((p.N + kBK - 1) / kBK));
+  kern<<<grid, kMainThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmdO, tmDQ, p);
+  return cudaGetLastError();
+}
+
 template <int D>
 cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
                    const CUtensorMap& tmdO, const CUtensorMap& tmDQ, const BwdParams& p,
                    unsigned stages, cudaStream_t stream) {
-  using C = Bwd<D>;
   int dev = 0, sms = 148;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -654,21 +718,9 @@ cudaError_t launch(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtenso
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & kBwdMain) {
-    auto kern = bwd_main_kernel<D>;
-    // setmaxnreg moves registers inside the launch allocation; refuse to launch
-    // if the compiler gave the kernel a different per-thread count than assumed.
-    static int regs = -1;
-    if (regs < 0) {
-      cudaFuncAttributes fa;
-      if ((e = cudaFuncGetAttributes(&fa, kern)) != cudaSuccess) return e;
-      regs = fa.numRegs;
-    }
-    if (regs != kLaunchRegs) return cudaErrorInvalidKernelImage;
-    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    e = p.bmask ? launch_main<D, true>(tmQ, tmK, tmV, tmdO, tmDQ, p, stream)
+                : launch_main<D, false>(tmQ, tmK, tmV, tmdO, tmDQ, p, stream);
     if (e != cudaSuccess) return e;
-    dim3 grid(p.B * p.Hkv * ((p.N + kBK - 1) / kBK));
-    kern<<<grid, kMainThreads, C::SMEM_BYTES, stream>>>(tmQ, tmK, tmV, tmdO, tmDQ, p);
-    if ((e = cudaGetLastError()) != cudaSuccess) return e;
   }
   if (stages & kBwdConvert) {
     const long long warps = (long long)p.B * p.Hq * p.Npad / kRowsPerWarp;
