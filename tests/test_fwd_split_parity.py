@@ -61,6 +61,12 @@ CASES = [
     (1, 16, 1, 9, 1000, 128, True, 2),    # 144 rows: not packed
     (1, 4, 1, 20, 10, 64, True, 1),       # packed, Nq > Nk: rows i < 10 keep no key
     (1, 32, 8, 1, 131072, 128, True, 0),  # the decode benchmark shape
+    # Few rows per kv head (decoding shapes), d = 64 and 128.
+    (2, 4, 4, 3, 1000, 64, True, 0),      # Hq == Hkv, 3 query rows
+    (1, 8, 1, 1, 5000, 64, False, 0),     # 8 packed rows, d = 64
+    (1, 2, 2, 8, 300, 128, True, 2),      # Hq == Hkv, 8 rows, bottom-right causal
+    (1, 6, 2, 2, 2000, 128, True, 0),     # 6 packed rows
+    (1, 4, 2, 1, 1, 128, False, 0),       # a single key
 ]
 
 
