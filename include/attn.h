@@ -34,7 +34,8 @@
  * sizes, Hq % Hkv != 0, a scale that is not finite and positive, or an
  * unknown dtype;
  * ATTN_ERR_UNSUPPORTED for combinations the kernels do not implement
- * (d other than 64 or 128, fp32 backward, fp32 input with bf16 output);
+ * (d other than 64 or 128, fp32 backward, fp32 input with bf16 output, the
+ * FP8 forward with d other than 128, sizes past the grid or list limits);
  * ATTN_ERR_CUDA when a CUDA runtime call or launch fails.  There is no CPU
  * fallback.
  */
