@@ -16,6 +16,10 @@ Functions carry the C names:
 * ``attn_fwd_masked(Q, K, V, block_mask, scale, causal, out_dtype=None)`` and
   ``attn_bwd_masked(Q, K, V, O, dO, LSE, block_mask, scale, causal)``: block-sparse
   attention with a uint8 CUDA mask [1 or Hq, ceil(N/128), ceil(N/128)]
+* ``attn_quantize_fp8(X, transpose=False) -> (codes, scales)`` and
+  ``attn_fwd_fp8(Qc, q_scale, Kc, k_scale, Vtc, v_scale, scale, causal)``: e4m3
+  codes with one fp32 scale per 128-row block (V transposed) and the FP8
+  forward on them (d = 128); ``attn_fp8_vt_stride(N)``
 * ``attn_bwd(Q, K, V, O, dO, LSE, scale, causal) -> (dQ, dK, dV)``
 * ``attn_bwd_workspace_size(B, Hq, Hkv, N, d)``
 * ``attn_last_device_status(stream=None)``, ``attn_status_string(code)``
