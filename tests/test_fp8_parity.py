@@ -119,6 +119,9 @@ FWD_CASES = [
     (1, 2, 1, 128, True),
     (1, 1, 1, 77, False),
     (1, 2, 2, 1536, True),
+    (1, 2, 1, 1, True),     # one query and one key
+    (1, 1, 1, 16, True),    # one partial tile
+    (2, 4, 1, 257, True),   # GQA 4:1, a tile of one row at the end
 ]
 
 
