@@ -18,6 +18,11 @@ Recipe
   (no intermediate fp32 rounding).  fp32 tensors are rounded once to fp32.
 * Tensor seeds: 0x5EED0000 + 16 * config_id + tensor_id with Q=0, K=1, V=2,
   dO=3.  The long-logit workload multiplies the rounded Q by 8 (exact in bf16).
+* Block-varying magnitudes (FP8 block quantization tests): every 128 rows
+  of a head multiplied by 2^e, e drawn uniformly from a small set by
+  SplitMix64 from the seed xor 0xB10C (exact: powers of two).
+* Block masks (block-sparse workloads): entry kept when a SplitMix64 uniform
+  is below the density.
 
 The named workloads are the five shapes the library is measured and checked
 on (see ``WORKLOADS``).
