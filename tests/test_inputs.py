@@ -81,3 +81,26 @@ def test_sample_rows():
 def test_make_tensor_rejects_inexact_multiplier():
     with pytest.raises(ValueError):
         inputs.make_tensor(1, (4,), "bf16", mul=3.0)
+
+
+def test_blocky_tensor_is_exact_and_seeded():
+    a = inputs.make_blocky_tensor(7, (2, 3, 300, 16), exps=(-2, 0, 3))
+    b = inputs.make_blocky_tensor(7, (2, 3, 300, 16), exps=(-2, 0, 3))
+    assert np.array_equal(a, b)
+    base = inputs.bf16_bits_to_f64(inputs.make_tensor(7, (2, 3, 300, 16), "bf16"))
+    x = inputs.bf16_bits_to_f64(a)
+    # Each 128-row block is the base times one power of two from the set.
+    ratio = x.reshape(6, 300, 16) / base.reshape(6, 300, 16)
+    for h in range(6):
+        for t in range(3):
+            r = np.unique(ratio[h, 128 * t:128 * (t + 1)])
+            assert r.size == 1 and r[0] in (0.25, 1.0, 8.0)
+
+
+def test_random_block_mask_density_and_seed():
+    m = inputs.random_block_mask(11, 2, 64, 0.5)
+    assert m.dtype == np.uint8 and m.shape == (2, 64, 64)
+    assert np.array_equal(m, inputs.random_block_mask(11, 2, 64, 0.5))
+    assert abs(m.mean() - 0.5) < 0.02
+    assert inputs.random_block_mask(11, 1, 8, 0.0).sum() == 0
+    assert inputs.random_block_mask(11, 1, 8, 1.0).sum() == 64
