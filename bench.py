@@ -366,29 +366,6 @@ def run_native(args):
                 "frac": dom_tf / sustained, "traffic": traffic, "kernel": dom,
                 "peak_source": f"bf16_tflops_sustained of {peak_src}"}
 
-    # The backward main kernel's shared-memory roofline (derived, not
-    # measured): per 128-key x 128-query step the SS products read both
-    # operands from shared memory, the TS products their B operand, and the
-    # step also loads Q and dO, stores dS, stages dQ and has it read by the
-    # reduce.  Peak: 128 B per clock per SM at the maximum SM clock.
-    if main_avg >= fwd_avg:
-        T = (w.N + 127) // 128
-        G = w.Hq // w.Hkv
-        steps = w.B * w.Hkv * G * (T * (T + 1) // 2 if w.causal else T * T)
-        d = w.d
-        per_step = (512 * d * 2          # S^T = K Q^T and dP^T = V dO^T (A and B)
-                    + 256 * d * 2        # dV += P^T dO and dK += dS^T Q (B)
-                    + 256 * max(d, 128) + 32768  # dQ^T = K^T dS^T (A padded to 128 rows, B)
-                    + 256 * d * 2        # Q and dO loads
-                    + 32768              # dS^T stored for dQ^T
-                    + 512 * d * 2)       # dQ staged, then read by the reduce
-        smem_peak = 128.0 * props.multi_processor_count * float(peaks.get("sm_max_mhz", 2070.0)) * 1e6 / 1e12
-        smem_tbps = steps * per_step / (main_avg / 1e3) / 1e12
-        roofline["secondary"] = {"bound": "smem", "achieved": smem_tbps, "peak": smem_peak, "unit": "TB/s",
-                                 "frac": smem_tbps / smem_peak, "bytes_per_launch": steps * per_step,
-                                 "note": "derived from the kernel's operand and staging traffic; "
-                                         "peak = 128 B/clk/SM x SMs x max SM clock"}
-
     e2e = run_e2e(args, pkg, w, t_np, dev, stream, ffl + bfl, world)
     # The secondary ceiling: one exponential per kept score, in the forward
     # and again in the backward's recomputation of P.
