@@ -224,3 +224,22 @@ def test_nonpositive_scale_is_rejected(lib):
     # The kernels take the row max on the unscaled scores: the scale must be > 0.
     assert _fwd(lib, scale=0.0) == pkg.ATTN_ERR_INVALID_ARG
     assert _fwd(lib, scale=-1.0) == pkg.ATTN_ERR_INVALID_ARG
+
+
+def test_binding_rejects_host_and_mistyped_tensors():
+    # The Python layer checks placement, dtype, shape and contiguity before
+    # any call reaches the library (no GPU needed for these paths).
+    import torch
+    x = torch.zeros(1, 2, 8, 128, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        pkg.attn_fwd(x, x, x, 0.1, True)  # host tensors
+    with pytest.raises(TypeError):
+        pkg.attn_fwd(x.int(), x, x, 0.1, True)  # unsupported dtype
+    with pytest.raises(TypeError):
+        pkg.attn_quantize_fp8(x)  # host tensor
+    codes = torch.zeros(1, 2, 8, 128, dtype=torch.uint8)
+    sc = torch.ones(1, 2, 1)
+    with pytest.raises(TypeError):
+        pkg.attn_fwd_fp8(codes, sc, codes, sc, codes, sc, 0.1, True)
+    with pytest.raises(TypeError):
+        pkg.attn_fwd_masked(x, x, x, torch.ones(1, 1, 1, dtype=torch.uint8), 0.1, True)
