@@ -119,15 +119,41 @@ def _ptr(t):
     return ctypes.c_void_p(t.data_ptr())
 
 
-def _check_tensor(name, t, dtype, shape):
+def _check_tensor(name, t, dtype, shape, device=None):
+    """Placement, dtype, shape and contiguity of a tensor handed to the library.
+
+    Outputs are checked like inputs: a host tensor, a wrong dtype or shape
+    would otherwise become a kernel's write target."""
     if not isinstance(t, torch.Tensor) or not t.is_cuda:
         raise TypeError(f"{name} must be a CUDA tensor")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
     if t.dtype != dtype:
         raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
     if not t.is_contiguous():
         raise ValueError(f"{name} must be contiguous")
+
+
+def _check_workspace(ws, need, device):
+    """A caller-given workspace: contiguous uint8 CUDA memory on `device`, at
+    least `need` bytes."""
+    if not isinstance(ws, torch.Tensor) or not ws.is_cuda:
+        raise TypeError("workspace must be a CUDA tensor")
+    if ws.device != device:
+        raise ValueError(f"workspace is on {ws.device}, expected {device}")
+    if ws.dtype != torch.uint8 or not ws.is_contiguous():
+        raise TypeError("workspace must be a contiguous uint8 tensor")
+    if ws.numel() < need:
+        raise ValueError(f"workspace has {ws.numel()} bytes, needs {need}")
+
+
+def _check_bwd_outputs(dQ, dK, dV, B, Hq, Hkv, N, d, device):
+    bf = torch.bfloat16
+    _check_tensor("dQ", dQ, bf, (B, Hq, N, d), device)
+    _check_tensor("dK", dK, bf, (B, Hkv, N, d), device)
+    _check_tensor("dV", dV, bf, (B, Hkv, N, d), device)
 
 
 def attn_status_string(code: int) -> str:
@@ -160,16 +186,18 @@ def attn_fwd(Q, K, V, scale=None, causal=False, out_dtype=None, O=None, LSE=None
         out_dtype = Q.dtype
     out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
     _check_tensor("Q", Q, Q.dtype, (B, Hq, N, d))
-    _check_tensor("K", K, Q.dtype, (B, Hkv, N, d))
-    _check_tensor("V", V, Q.dtype, (B, Hkv, N, d))
+    dev = Q.device
+    _check_tensor("K", K, Q.dtype, (B, Hkv, N, d), dev)
+    _check_tensor("V", V, Q.dtype, (B, Hkv, N, d), dev)
     if O is None:
-        O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Q.device)
+        O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=dev)
     if LSE is None:
-        LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device)
-    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
-    rc = lib.attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
-                      float(scale), int(bool(causal)), in_dt, out_dt, _stream(stream))
+        LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=dev)
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d), dev)
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N), dev)
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d,
+                          float(scale), int(bool(causal)), in_dt, out_dt, _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd")
     return O, LSE
@@ -196,31 +224,37 @@ def attn_fwd_split(Q, K, V, scale=None, causal=False, num_splits=0, out_dtype=No
         out_dtype = bf
     out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
     _check_tensor("Q", Q, bf, (B, Hq, Nq, d))
-    _check_tensor("K", K, bf, (B, Hkv, Nk, d))
-    _check_tensor("V", V, bf, (B, Hkv, Nk, d))
+    dev = Q.device
+    _check_tensor("K", K, bf, (B, Hkv, Nk, d), dev)
+    _check_tensor("V", V, bf, (B, Hkv, Nk, d), dev)
     if O is None:
-        O = torch.empty((B, Hq, Nq, d), dtype=out_dtype, device=Q.device)
+        O = torch.empty((B, Hq, Nq, d), dtype=out_dtype, device=dev)
     if LSE is None:
-        LSE = torch.empty((B, Hq, Nq), dtype=torch.float32, device=Q.device)
-    _check_tensor("O", O, out_dtype, (B, Hq, Nq, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, Nq))
+        LSE = torch.empty((B, Hq, Nq), dtype=torch.float32, device=dev)
+    _check_tensor("O", O, out_dtype, (B, Hq, Nq, d), dev)
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, Nq), dev)
     ws_bytes = attn_fwd_split_workspace_size(B, Hq, Hkv, Nq, Nk, d, num_splits)
     if workspace is None and ws_bytes > 0:
-        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=Q.device)
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    if workspace is not None:
+        _check_workspace(workspace, ws_bytes, dev)
     wptr = _ptr(workspace) if workspace is not None else ctypes.c_void_p(0)
-    wbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
-    rc = lib.attn_fwd_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, Nq, Nk, d,
-                            float(scale), int(bool(causal)), out_dt, int(num_splits), wptr, wbytes,
-                            _stream(stream))
+    wbytes = workspace.numel() if workspace is not None else 0
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_split(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, Nq, Nk, d,
+                                float(scale), int(bool(causal)), out_dt, int(num_splits), wptr, wbytes,
+                                _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_split")
     return O, LSE
 
 
-def _check_mask(block_mask, Hq, N):
+def _check_mask(block_mask, Hq, N, device):
     T = (N + 127) // 128
     if not isinstance(block_mask, torch.Tensor) or not block_mask.is_cuda or block_mask.dtype != torch.uint8:
         raise TypeError("block_mask must be a uint8 CUDA tensor")
+    if block_mask.device != device:
+        raise ValueError(f"block_mask is on {block_mask.device}, expected {device}")
     m = block_mask if block_mask.dim() == 3 else block_mask.reshape(1, T, T)
     if tuple(m.shape[1:]) != (T, T) or m.shape[0] not in (1, Hq) or not m.is_contiguous():
         raise ValueError(f"block_mask must be contiguous [1 or {Hq}, {T}, {T}], got {tuple(block_mask.shape)}")
@@ -239,15 +273,18 @@ def attn_fwd_masked(Q, K, V, block_mask, scale=None, causal=False, out_dtype=Non
     bf = torch.bfloat16
     out_dtype = bf if out_dtype is None else out_dtype
     out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
-    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv)):
-        _check_tensor(name, t, bf, (B, H, N, d))
-    m, mh = _check_mask(block_mask, Hq, N)
-    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Q.device) if O is None else O
-    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=Q.device) if LSE is None else LSE
-    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
-    rc = lib.attn_fwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, float(scale),
-                             int(bool(causal)), _ptr(m), mh, out_dt, _stream(stream))
+    _check_tensor("Q", Q, bf, (B, Hq, N, d))
+    dev = Q.device
+    for name, t, H in (("K", K, Hkv), ("V", V, Hkv)):
+        _check_tensor(name, t, bf, (B, H, N, d), dev)
+    m, mh = _check_mask(block_mask, Hq, N, dev)
+    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=dev) if O is None else O
+    LSE = torch.empty((B, Hq, N), dtype=torch.float32, device=dev) if LSE is None else LSE
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d), dev)
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N), dev)
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, float(scale),
+                                 int(bool(causal)), _ptr(m), mh, out_dt, _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_masked")
     return O, LSE
@@ -266,14 +303,16 @@ def attn_quantize_fp8(X, transpose=False, codes=None, scales=None, stream=None):
     lib = load_library()
     B, H, N, d = X.shape
     _check_tensor("X", X, torch.bfloat16, (B, H, N, d))
+    dev = X.device
     T = (N + 127) // 128
     cshape = (B, H, d, attn_fp8_vt_stride(N)) if transpose else (B, H, N, d)
-    codes = torch.empty(cshape, dtype=torch.uint8, device=X.device) if codes is None else codes
-    scales = torch.empty((B, H, T), dtype=torch.float32, device=X.device) if scales is None else scales
-    _check_tensor("codes", codes, torch.uint8, cshape)
-    _check_tensor("scales", scales, torch.float32, (B, H, T))
-    rc = lib.attn_quantize_fp8(_ptr(X), _ptr(codes), _ptr(scales), B * H, N, d, int(bool(transpose)),
-                               _stream(stream))
+    codes = torch.empty(cshape, dtype=torch.uint8, device=dev) if codes is None else codes
+    scales = torch.empty((B, H, T), dtype=torch.float32, device=dev) if scales is None else scales
+    _check_tensor("codes", codes, torch.uint8, cshape, dev)
+    _check_tensor("scales", scales, torch.float32, (B, H, T), dev)
+    with torch.cuda.device(dev):
+        rc = lib.attn_quantize_fp8(_ptr(X), _ptr(codes), _ptr(scales), B * H, N, d, int(bool(transpose)),
+                                   _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_quantize_fp8")
     return codes, scales
@@ -292,44 +331,58 @@ def attn_fwd_fp8(Qc, q_scale, Kc, k_scale, Vtc, v_scale, scale=None, causal=Fals
     out_dt = {torch.bfloat16: ATTN_BF16, torch.float32: ATTN_F32}[out_dtype]
     u8, f32 = torch.uint8, torch.float32
     _check_tensor("Qc", Qc, u8, (B, Hq, N, d))
-    _check_tensor("Kc", Kc, u8, (B, Hkv, N, d))
-    _check_tensor("Vtc", Vtc, u8, (B, Hkv, d, attn_fp8_vt_stride(N)))
-    _check_tensor("q_scale", q_scale, f32, (B, Hq, T))
-    _check_tensor("k_scale", k_scale, f32, (B, Hkv, T))
-    _check_tensor("v_scale", v_scale, f32, (B, Hkv, T))
-    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=Qc.device) if O is None else O
-    LSE = torch.empty((B, Hq, N), dtype=f32, device=Qc.device) if LSE is None else LSE
-    _check_tensor("O", O, out_dtype, (B, Hq, N, d))
-    _check_tensor("LSE", LSE, f32, (B, Hq, N))
-    rc = lib.attn_fwd_fp8(_ptr(Qc), _ptr(q_scale), _ptr(Kc), _ptr(k_scale), _ptr(Vtc), _ptr(v_scale), _ptr(O),
-                          _ptr(LSE), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), out_dt, _stream(stream))
+    dev = Qc.device
+    _check_tensor("Kc", Kc, u8, (B, Hkv, N, d), dev)
+    _check_tensor("Vtc", Vtc, u8, (B, Hkv, d, attn_fp8_vt_stride(N)), dev)
+    _check_tensor("q_scale", q_scale, f32, (B, Hq, T), dev)
+    _check_tensor("k_scale", k_scale, f32, (B, Hkv, T), dev)
+    _check_tensor("v_scale", v_scale, f32, (B, Hkv, T), dev)
+    O = torch.empty((B, Hq, N, d), dtype=out_dtype, device=dev) if O is None else O
+    LSE = torch.empty((B, Hq, N), dtype=f32, device=dev) if LSE is None else LSE
+    _check_tensor("O", O, out_dtype, (B, Hq, N, d), dev)
+    _check_tensor("LSE", LSE, f32, (B, Hq, N), dev)
+    with torch.cuda.device(dev):
+        rc = lib.attn_fwd_fp8(_ptr(Qc), _ptr(q_scale), _ptr(Kc), _ptr(k_scale), _ptr(Vtc), _ptr(v_scale),
+                              _ptr(O), _ptr(LSE), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), out_dt,
+                              _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_fwd_fp8")
     return O, LSE
+
+
+def _bwd_inputs(Q, K, V, O, dO, LSE):
+    """Checks the backward's inputs; returns (B, Hq, Hkv, N, d, device)."""
+    B, Hq, N, d = Q.shape
+    Hkv = K.shape[1]
+    bf = torch.bfloat16
+    _check_tensor("Q", Q, bf, (B, Hq, N, d))
+    dev = Q.device
+    for name, t, H in (("K", K, Hkv), ("V", V, Hkv), ("O", O, Hq), ("dO", dO, Hq)):
+        _check_tensor(name, t, bf, (B, H, N, d), dev)
+    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N), dev)
+    return B, Hq, Hkv, N, d, dev
 
 
 def attn_bwd_masked(Q, K, V, O, dO, LSE, block_mask, scale=None, causal=False, dQ=None, dK=None, dV=None,
                     workspace=None, stream=None):
     """Block-sparse backward with the mask of attn_fwd_masked."""
     lib = load_library()
-    B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, Hq, Hkv, N, d, dev = _bwd_inputs(Q, K, V, O, dO, LSE)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    bf = torch.bfloat16
-    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv), ("O", O, Hq), ("dO", dO, Hq)):
-        _check_tensor(name, t, bf, (B, H, N, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
-    m, mh = _check_mask(block_mask, Hq, N)
+    m, mh = _check_mask(block_mask, Hq, N, dev)
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
+    _check_bwd_outputs(dQ, dK, dV, B, Hq, Hkv, N, d, dev)
+    ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d)
     if workspace is None:
-        workspace = torch.empty(max(attn_bwd_workspace_size(B, Hq, Hkv, N, d), 1), dtype=torch.uint8,
-                                device=Q.device)
-    rc = lib.attn_bwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
-                             _ptr(dV), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), _ptr(m), mh,
-                             _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream))
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check_workspace(workspace, ws_bytes, dev)
+    with torch.cuda.device(dev):
+        rc = lib.attn_bwd_masked(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK),
+                                 _ptr(dV), B, Hq, Hkv, N, d, float(scale), int(bool(causal)), _ptr(m), mh,
+                                 _ptr(workspace), workspace.numel(), _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd_masked")
     return dQ, dK, dV
@@ -343,28 +396,23 @@ def attn_bwd(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=None, dV
     "preprocess", "main", "convert" (run in that order with the same
     workspace to obtain the same result)."""
     lib = load_library()
-    B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, Hq, Hkv, N, d, dev = _bwd_inputs(Q, K, V, O, dO, LSE)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    bf = torch.bfloat16
-    _check_tensor("Q", Q, bf, (B, Hq, N, d))
-    _check_tensor("K", K, bf, (B, Hkv, N, d))
-    _check_tensor("V", V, bf, (B, Hkv, N, d))
-    _check_tensor("O", O, bf, (B, Hq, N, d))
-    _check_tensor("dO", dO, bf, (B, Hq, N, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
+    _check_bwd_outputs(dQ, dK, dV, B, Hq, Hkv, N, d, dev)
     ws_bytes = attn_bwd_workspace_size(B, Hq, Hkv, N, d)
     if workspace is None:
-        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=Q.device)
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _check_workspace(workspace, ws_bytes, dev)
     fname = _BWD_STAGES[stage]
-    rc = getattr(lib, fname)(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
-                             _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, float(scale),
-                             int(bool(causal)), ATTN_BF16, _ptr(workspace),
-                             workspace.numel() * workspace.element_size(), _stream(stream))
+    with torch.cuda.device(dev):
+        rc = getattr(lib, fname)(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ),
+                                 _ptr(dK), _ptr(dV), B, Hq, Hkv, N, d, float(scale),
+                                 int(bool(causal)), ATTN_BF16, _ptr(workspace), workspace.numel(),
+                                 _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, fname)
     return dQ, dK, dV
@@ -389,19 +437,16 @@ def attn_bwd_noalloc(Q, K, V, O, dO, LSE, scale=None, causal=False, dQ=None, dK=
     vp, i32, f32 = ctypes.c_void_p, ctypes.c_int, ctypes.c_float
     fn.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, f32, i32, i32, vp]
     fn.restype = i32
-    B, Hq, N, d = Q.shape
-    Hkv = K.shape[1]
+    B, Hq, Hkv, N, d, dev = _bwd_inputs(Q, K, V, O, dO, LSE)
     if scale is None:
         scale = 1.0 / math.sqrt(d)
-    bf = torch.bfloat16
-    for name, t, H in (("Q", Q, Hq), ("K", K, Hkv), ("V", V, Hkv), ("O", O, Hq), ("dO", dO, Hq)):
-        _check_tensor(name, t, bf, (B, H, N, d))
-    _check_tensor("LSE", LSE, torch.float32, (B, Hq, N))
     dQ = torch.empty_like(Q) if dQ is None else dQ
     dK = torch.empty_like(K) if dK is None else dK
     dV = torch.empty_like(V) if dV is None else dV
-    rc = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
-            B, Hq, Hkv, N, d, float(scale), int(bool(causal)), ATTN_BF16, _stream(stream))
+    _check_bwd_outputs(dQ, dK, dV, B, Hq, Hkv, N, d, dev)
+    with torch.cuda.device(dev):
+        rc = fn(_ptr(Q), _ptr(K), _ptr(V), _ptr(O), _ptr(dO), _ptr(LSE), _ptr(dQ), _ptr(dK), _ptr(dV),
+                B, Hq, Hkv, N, d, float(scale), int(bool(causal)), ATTN_BF16, _stream(stream))
     if rc != ATTN_OK:
         raise AttnError(rc, "attn_bwd_noalloc")
     return dQ, dK, dV

@@ -41,6 +41,15 @@ extern "C" attn_status attn_bwd_noalloc(const void* Q, const void* K, const void
                                         const void* dO, const float* LSE, void* dQ, void* dK,
                                         void* dV, int B, int Hq, int Hkv, int N, int d, float scale,
                                         int causal, attn_dtype dtype, void* stream) {
+  // The checks attn_bwd makes before it looks at sizes come first, so that a
+  // null, misaligned or mistyped argument gets the same status from both
+  // entry points, whatever the sizes.
+  if (!Q || !K || !V || !O || !dO || !LSE || !dQ || !dK || !dV) return ATTN_ERR_INVALID_ARG;
+  if (dtype != ATTN_BF16 && dtype != ATTN_F32) return ATTN_ERR_INVALID_ARG;
+  const void* ptrs[] = {Q, K, V, O, dO, dQ, dK, dV};
+  for (const void* q : ptrs)
+    if (reinterpret_cast<uintptr_t>(q) % 16 != 0) return ATTN_ERR_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return ATTN_ERR_INVALID_ARG;
   const size_t need = attn_bwd_workspace_size(B, Hq, Hkv, N, d);
   if (need > (size_t)ATTN_NOALLOC_SCRATCH_BYTES) return ATTN_ERR_UNSUPPORTED;
   if (need == 0) {

@@ -235,7 +235,9 @@ attn_status attn_bwd_convert(const void* Q, const void* K, const void* V, const 
  * Arguments and results are those of attn_bwd.  The scratch memory is a fixed
  * array of ATTN_NOALLOC_SCRATCH_BYTES bytes compiled into the library; every
  * GPU that loads the library holds it until the process exits.  Problems whose
- * attn_bwd_workspace_size() exceeds it return ATTN_ERR_UNSUPPORTED.  The call
+ * attn_bwd_workspace_size() exceeds it return ATTN_ERR_UNSUPPORTED; null,
+ * misaligned or mistyped arguments are reported first, with attn_bwd's
+ * ATTN_ERR_INVALID_ARG, whatever the sizes.  The call
  * allocates nothing.  The first call on a device looks up the array's device
  * address (cudaGetSymbolAddress, with that device current); make that first
  * call before any stream capture.  All calls on a device share the array and

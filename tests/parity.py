@@ -8,9 +8,12 @@ Tolerances (the stated bars):
                dQ, dK, dV: max-abs error / max-abs reference <= 2e-2.
 """
 
+import functools
+
 import numpy as np
 import torch
 
+import oracle
 from exact_attention_95_gb300 import inputs
 
 O_TOL = 1e-2
@@ -56,3 +59,17 @@ def check_o(o_gpu: np.ndarray, o_ref: np.ndarray, bf16_out: bool, tol=O_TOL):
 def rel_err(x: np.ndarray, ref: np.ndarray) -> float:
     den = float(np.abs(ref).max())
     return float(np.abs(x - ref).max()) / den if den > 0 else float(np.abs(x).max())
+
+
+@functools.lru_cache(maxsize=2)
+def workload_reference(name):
+    """The seeded inputs of a named workload and the oracle's full fp64 forward
+    and backward on them: (workload, inputs as stored, oracle result dict with
+    O, LSE, D, dQ, dK, dV).  Cached, because the causal d=128 workload costs
+    tens of seconds on the host cores and both the forward and the backward
+    tests compare against it."""
+    w = inputs.WORKLOADS[name]
+    t = inputs.workload_tensors(w)
+    f = {k: inputs.to_f64(v) for k, v in t.items()}
+    ref = oracle.bwd(f["Q"], f["K"], f["V"], f["dO"], w.scale, w.causal)
+    return w, t, ref

@@ -243,3 +243,47 @@ def test_binding_rejects_host_and_mistyped_tensors():
         pkg.attn_fwd_fp8(codes, sc, codes, sc, codes, sc, 0.1, True)
     with pytest.raises(TypeError):
         pkg.attn_fwd_masked(x, x, x, torch.ones(1, 1, 1, dtype=torch.uint8), 0.1, True)
+
+
+def test_binding_rejects_bad_backward_outputs_and_workspace():
+    # Outputs and the workspace become kernel write targets: they are checked
+    # like inputs.  On a machine without a GPU the helpers are called directly.
+    import torch
+    x = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16)
+    with pytest.raises(TypeError):
+        pkg.attn_bwd(x, x, x, x, x, torch.zeros(1, 2, 8), 0.1, True)  # host inputs
+    with pytest.raises(TypeError):
+        pkg._check_bwd_outputs(x, x, x, 1, 2, 2, 8, 64, None)  # host dQ
+    with pytest.raises(TypeError):
+        pkg._check_workspace(torch.zeros(16, dtype=torch.uint8), 16, None)  # host workspace
+    with pytest.raises(TypeError):
+        pkg.attn_bwd_noalloc(x, x, x, x, x, torch.zeros(1, 2, 8), 0.1, True)
+    with pytest.raises(TypeError):
+        pkg.attn_bwd_masked(x, x, x, x, x, torch.zeros(1, 2, 8), torch.ones(1, 1, 1, dtype=torch.uint8),
+                            0.1, True)
+
+
+@pytest.mark.gpu
+def test_binding_rejects_bad_backward_outputs_on_gpu():
+    import torch
+    dev = torch.device("cuda")
+    q = torch.zeros(1, 2, 8, 64, dtype=torch.bfloat16, device=dev)
+    lse = torch.zeros(1, 2, 8, device=dev)
+    good = dict(dQ=torch.empty_like(q), dK=torch.empty_like(q), dV=torch.empty_like(q))
+    bad_cases = [
+        (TypeError, dict(dQ=torch.empty(1, 2, 8, 64, dtype=torch.bfloat16))),        # host output
+        (TypeError, dict(dK=torch.empty(1, 2, 8, 64, dtype=torch.float32, device=dev))),  # fp32 output
+        (ValueError, dict(dV=torch.empty(1, 2, 8, 32, dtype=torch.bfloat16, device=dev))),  # wrong shape
+        (TypeError, dict(workspace=torch.empty(1 << 20, dtype=torch.uint8))),       # host workspace
+        (TypeError, dict(workspace=torch.empty(1 << 18, dtype=torch.float32, device=dev))),
+        (ValueError, dict(workspace=torch.empty(16, dtype=torch.uint8, device=dev))),  # too small
+    ]
+    for exc, kw in bad_cases:
+        args = dict(good, **kw)
+        with pytest.raises(exc):
+            pkg.attn_bwd(q, q, q, q, q, lse, 0.125, True, **args)
+        if "workspace" not in kw:
+            with pytest.raises(exc):
+                pkg.attn_bwd_noalloc(q, q, q, q, q, lse, 0.125, True, **args)
+    with pytest.raises(TypeError):
+        pkg.attn_fwd(q, q, q, 0.125, True, O=torch.empty(1, 2, 8, 64, dtype=torch.bfloat16))

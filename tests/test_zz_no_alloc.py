@@ -65,6 +65,31 @@ def test_noalloc_rejects_sizes_beyond_its_scratch():
     assert pkg.attn_bwd_workspace_size(B, Hq, Hkv, N, d) > pkg.NOALLOC_SCRATCH_BYTES
     rc = fn(A, A, A, A, A, A, A, A, A, B, Hq, Hkv, N, d, 0.1, 1, pkg.ATTN_BF16, None)
     assert rc == pkg.ATTN_ERR_UNSUPPORTED
+    # A null or misaligned argument is reported as attn_bwd reports it, before
+    # the size limit.
+    assert fn(None, A, A, A, A, A, A, A, A, B, Hq, Hkv, N, d, 0.1, 1, pkg.ATTN_BF16, None) == \
+        pkg.ATTN_ERR_INVALID_ARG
+    assert fn(A, A, A, A, A, A, ctypes.c_void_p(0x10008), A, A, B, Hq, Hkv, N, d, 0.1, 1, pkg.ATTN_BF16,
+              None) == pkg.ATTN_ERR_INVALID_ARG
+    assert fn(A, A, A, A, A, A, A, A, A, B, Hq, Hkv, N, d, 0.1, 1, 9, None) == pkg.ATTN_ERR_INVALID_ARG
     # Invalid sizes still get attn_bwd's own error codes.
     assert fn(A, A, A, A, A, A, A, A, A, 1, 3, 2, 64, 128, 0.1, 1, 0, None) == pkg.ATTN_ERR_INVALID_ARG
     assert fn(A, A, A, A, A, A, A, A, A, 1, 2, 2, 64, 96, 0.1, 1, 0, None) == pkg.ATTN_ERR_UNSUPPORTED
+
+
+def test_noalloc_python_wrapper_matches_workspace_backward():
+    # The same comparison through the package's wrapper (argument checks,
+    # current stream), twice in a row.
+    B, Hq, Hkv, N, d, causal = 1, 2, 1, 257, 128, True
+    t = make(B, Hq, Hkv, N, d, seed=8900)
+    g = {k: to_dev(v) for k, v in t.items()}
+    scale = 1.0 / np.sqrt(d)
+    O, L = pkg.attn_fwd(g["Q"], g["K"], g["V"], scale, causal)
+    ref = pkg.attn_bwd(g["Q"], g["K"], g["V"], O, g["dO"], L, scale, causal)
+    for _ in range(2):
+        out = pkg.attn_bwd_noalloc(g["Q"], g["K"], g["V"], O, g["dO"], L, scale, causal)
+        torch.cuda.synchronize()
+        assert pkg.attn_last_device_status() == pkg.ATTN_OK
+        for name, x, r in zip(("dQ", "dK", "dV"), out, ref):
+            e = rel_err(f64(x), f64(r))
+            assert e <= GRAD_TOL, f"{name} rel err {e:.3e}"
