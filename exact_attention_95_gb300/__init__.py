@@ -39,7 +39,12 @@ import threading
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libattn_sm103.so")
+# ATTN_DEBUG=1 selects the debug build (python -m exact_attention_95_gb300.build
+# --debug): the same kernels with explicit bounds checks on tensor-copy
+# coordinates and store indices, reported through attn_last_device_status as
+# ATTN_ERR_DEVICE instead of an access out of bounds.
+LIB_PATH = os.path.join(_HERE, "libattn_sm103_debug.so" if os.environ.get("ATTN_DEBUG") == "1"
+                        else "libattn_sm103.so")
 
 ATTN_OK, ATTN_ERR_INVALID_ARG, ATTN_ERR_UNSUPPORTED = 0, 1, 2
 ATTN_ERR_CUDA, ATTN_ERR_TIMEOUT, ATTN_ERR_DEVICE = 3, 4, 5

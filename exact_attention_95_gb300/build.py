@@ -18,6 +18,11 @@ CSRC = os.path.join(HERE, "csrc")
 ROOT = os.path.dirname(HERE)
 LIB = os.path.join(HERE, "libattn_sm103.so")
 BUILD = os.path.join(HERE, "_build")
+# Debug variant: the same sources with -DATTN_DEBUG (explicit bounds checks on
+# tensor-copy coordinates and store indices that record a device status
+# instead of trapping), built next to the release library.
+DEBUG_LIB = os.path.join(HERE, "libattn_sm103_debug.so")
+DEBUG_BUILD = os.path.join(HERE, "_build_debug")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
          "-I", os.path.join(ROOT, "include")]
@@ -39,21 +44,25 @@ def _deps():
         os.path.join(CSRC, "*.h")) + [os.path.join(ROOT, "include", "attn.h"), __file__]
 
 
-def up_to_date() -> bool:
-    if not os.path.exists(LIB):
+def up_to_date(lib: str = LIB) -> bool:
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(p) <= t for p in _deps())
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
-    if not force and up_to_date():
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, verbose: bool = False, extra_flags=(), debug: bool = False) -> str:
+    """Compile and link the library; with debug=True the -DATTN_DEBUG variant."""
+    lib, bdir = (DEBUG_LIB, DEBUG_BUILD) if debug else (LIB, BUILD)
+    if debug:
+        extra_flags = tuple(extra_flags) + ("-DATTN_DEBUG",)
+    if not force and up_to_date(lib):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     nvcc = _nvcc()
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+        obj = os.path.join(bdir, os.path.basename(src) + ".o")
         cmd = [nvcc, *ARCH, *FLAGS, *extra_flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -64,16 +73,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, _sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    build(force="--force" in sys.argv, verbose=True,
-          extra_flags=("-Xptxas", "-v") if "--ptxas-v" in sys.argv else ())
-    print(LIB)
+    print(build(force="--force" in sys.argv, verbose=True, debug="--debug" in sys.argv,
+                extra_flags=("-Xptxas", "-v") if "--ptxas-v" in sys.argv else ()))

@@ -15,6 +15,13 @@ namespace attn {
 // (atomicCAS from 0); attn_last_device_status reads and clears it.
 __device__ int g_status = 0;
 
+// Work counters of persistent launches: kSchedPairs pairs (next item, CTAs
+// finished) per device, 0 between launches (each launch's last CTA resets its
+// pair).  Launches take pairs in turn, so up to kSchedPairs launches may be
+// in flight at once (on any streams) without sharing a pair.
+constexpr int kSchedPairs = 64;
+__device__ unsigned g_sched[2 * kSchedPairs];
+
 namespace {
 
 constexpr unsigned long long kDefaultWaitLimitNs = 2000000000ull;  // 2 s per wait
@@ -51,6 +58,40 @@ int* status_ptr() {
     ptrs[dev] = static_cast<int*>(p);
   }
   return ptrs[dev];
+}
+
+}  // namespace
+
+unsigned* sched_counter_pair() {
+  static unsigned* base[64] = {};
+  static unsigned next[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lk(mu);
+  if (!base[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess) return nullptr;
+    base[dev] = static_cast<unsigned*>(p);
+  }
+  unsigned* pair = base[dev] + 2 * (next[dev] % kSchedPairs);
+  ++next[dev];
+  return pair;
+}
+
+namespace {
+
+// Streaming multiprocessors of the current device (cached per device).
+int sm_count() {
+  static int sms[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    sms[dev] = n;
+  }
+  return sms[dev];
 }
 
 // 3-D map over a bf16 [BH][N][d] tensor: box of 64 columns (128 bytes, the
@@ -241,7 +282,18 @@ attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, f
   p.causal = causal;
   p.out_f32 = out_f32;
   p.wait_limit_ns = wait_limit();
-  cudaError_t e = launch_fwd_bf16(d, tq, tk, tv, p, s);
+  cudaError_t e;
+  if (rows > 128 && !bmask) {
+    // Dense two-tile forward: persistent, one CTA per SM (its shared memory
+    // and TMEM allow one) over the items.
+    const int sms = sm_count();
+    p.sched = sched_counter_pair();
+    if (sms < 1 || !p.sched) return ATTN_ERR_CUDA;
+    p.n_items = (int)(heads * p.n_pairs * splits);
+    e = launch_fwd_persist(d, tq, tk, tv, p, std::min(p.n_items, sms), s);
+  } else {
+    e = launch_fwd_bf16(d, tq, tk, tv, p, s);
+  }
   return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA;
 }
 

@@ -360,10 +360,11 @@ __global__ void __launch_bounds__(kMainThreads, 1)
       tma_prefetch_desc(&tmV);
       tma_prefetch_desc(&tmdO);
       mbar_arrive_expect_tx(bar(C::B_KVFULL), 2 * C::CB * C::BLK);
-      for (int cb = 0; cb < C::CB; ++cb) {
-        tma_load_3d(sK + cb * C::BLK, &tmK, bar(C::B_KVFULL), cb * 64, k0, bhk);
-        tma_load_3d(sV + cb * C::BLK, &tmV, bar(C::B_KVFULL), cb * 64, k0, bhk);
-      }
+      if (dcheck(k0 >= 0 && k0 < p.N && bhk >= 0 && bhk < p.B * p.Hkv, p.status))
+        for (int cb = 0; cb < C::CB; ++cb) {
+          tma_load_3d(sK + cb * C::BLK, &tmK, bar(C::B_KVFULL), cb * 64, k0, bhk);
+          tma_load_3d(sV + cb * C::BLK, &tmV, bar(C::B_KVFULL), cb * 64, k0, bhk);
+        }
       int tq = 0, tdo = 0;  // Q parts and dO parts issued
       for (int t = 0; t < T; ++t) {
         const int s = t % C::STAGES;
@@ -374,9 +375,13 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const uint32_t st = stage(s);
         const uint32_t fb = bar(C::B_STFULL + s);
         mbar_arrive_expect_tx(fb, C::CB * C::BLK + 2 * kBQ * 4);
+        const size_t vo = (size_t)bhq * p.Npad + (size_t)it * kBQ;
+        if (!dcheck(it >= 0 && it * kBQ < p.N && bhq >= 0 && bhq < p.B * p.Hq &&
+                        vo + kBQ <= (size_t)p.B * p.Hq * p.Npad,
+                    p.status))
+          break;  // (debug builds only: the stage never fills; the waits on it time out)
         for (int cb = 0; cb < C::CB; ++cb)
           tma_load_3d(st + C::ST_Q + cb * C::BLK, &tmQ, fb, cb * 64, it * kBQ, bhq);
-        const size_t vo = (size_t)bhq * p.Npad + (size_t)it * kBQ;
         asm volatile(
             "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
                 st + C::ST_LSE),
@@ -481,6 +486,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
         const int bhq = b * p.Hq + hk * G + g;
         const uint32_t st = stage(s);
         const int row0 = (int)((size_t)bhq * p.Npad + (size_t)it * kBQ);
+        if (!dcheck(row0 >= 0 && (size_t)row0 + kBQ <= (size_t)p.B * p.Hq * p.Npad, p.status)) break;
         if (C::STAGED) {
           // The half in the dO slot first (the next loads wait for it), then
           // the half in the staging buffer.
@@ -655,7 +661,7 @@ __global__ void __launch_bounds__(kMainThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; ++i) o[i] = 0u;
           }
-          if (key_ok) {
+          if (key_ok && dcheck(row < (size_t)p.B * p.Hkv * p.N, p.status)) {
             uint4* d4 = reinterpret_cast<uint4*>(dst + col);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {

@@ -198,10 +198,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tmK);
       tma_prefetch_desc(&tmV);
       mbar_arrive_expect_tx(bar(C::B_QFULL), C::QT * C::TILE_BYTES);
-      for (int t = 0; t < C::QT; ++t)
-        for (int cb = 0; cb < C::CB; ++cb)
-          tma_load_3d(sQ + t * C::TILE_BYTES + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64,
-                      q0 + t * kBM, bh);
+      if (dcheck(q0 >= 0 && q0 < p.n_pairs * 2 * kBM && bh >= 0 && bh < p.heads, p.status))
+        for (int t = 0; t < C::QT; ++t)
+          for (int cb = 0; cb < C::CB; ++cb)
+            tma_load_3d(sQ + t * C::TILE_BYTES + cb * C::BLOCK_BYTES, &tmQ, bar(C::B_QFULL), cb * 64,
+                        q0 + t * kBM, bh);
       // Load order follows use order: K_0, then K_{j+1} before V_j (the next
       // Q K^T is issued before this tile's P V).
       int li = 0;
@@ -230,9 +231,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(bar(C::B_KVFULL + s), C::TILE_BYTES);
         const CUtensorMap* m = v ? &tmV : &tmK;
-        for (int cb = 0; cb < C::CB; ++cb)
-          tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
-                      ktile(j) * kBN, bh_kv);
+        const int kt = ktile(j);
+        if (dcheck(kt >= 0 && kt * kBN < p.Nk && bh_kv >= 0 && bh_kv < (p.packed ? p.heads : p.B * p.Hkv),
+                   p.status))
+          for (int cb = 0; cb < C::CB; ++cb)
+            tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
+                        kt * kBN, bh_kv);
       }
       // Drain: every issued copy must land before the CTA may exit.
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
@@ -467,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // between O and the divisor.  LSE uses the exact sum.
       const float lo = l - corr;
       const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
-      const bool valid = q < p.rows;
+      const bool valid = q < p.rows && dcheck(split < p.n_splits, p.status);
       const size_t row_idx = (size_t)bh * p.rows + q;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {

@@ -36,13 +36,27 @@ struct FwdParams {
   int causal;
   int out_f32;
   unsigned long long wait_limit_ns;
+  // Persistent launch: items = heads * n_pairs * n_splits handed out by the
+  // counter pair sched[0] (next item) and sched[1] (CTAs finished), both 0
+  // at launch and reset to 0 by the last CTA.
+  unsigned* sched;
+  int n_items;
 };
+
+// Counter pairs for persistent launches: a launch takes the next pair of a
+// small per-device pool, so that launches in flight on different streams do
+// not share one.
+unsigned* sched_counter_pair();
 
 // tcgen05 forward for bf16 inputs.  tmQ/tmK/tmV are 3-D maps over
 // [B*H][N][d] with a (64, 128, 1) box and 128-byte swizzle.
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
 size_t fwd_bf16_smem_bytes(int d);
+// Persistent form of the dense two-tile forward (rows > 128, no block mask):
+// `ctas` CTAs (at most one per SM) walk the p.n_items work items.
+cudaError_t launch_fwd_persist(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                               const FwdParams& p, int ctas, cudaStream_t stream);
 constexpr int kMaxMaskTiles = 2048;  // key tiles a block-sparse forward may list per CTA
 
 // Merge of a split forward's partial results: Opart [n_splits][rows][d] fp32

@@ -13,7 +13,28 @@ namespace attn {
 enum : int {
   kDevOk = 0,
   kDevTimeout = 1,  // a bounded mbarrier wait ran out
+  kDevBounds = 3,   // a debug-build bounds check failed (2 is the backward's alignment check)
 };
+
+// Debug builds (-DATTN_DEBUG) check the coordinates of tensor copies and the
+// indices of global stores explicitly.  A failed check records kDevBounds in
+// the status word (the first failure of the launch wins) and the access it
+// guards is skipped -- a skipped copy then leaves its barrier incomplete, and
+// the bounded wait on it returns with a timeout.  There is no trap.  Release
+// builds compile the checks away.
+#ifdef ATTN_DEBUG
+constexpr bool kDebugChecks = true;
+#else
+constexpr bool kDebugChecks = false;
+#endif
+__device__ __forceinline__ bool dcheck(bool ok, int* status) {
+  if constexpr (kDebugChecks) {
+    if (!ok) atomicCAS(status, kDevOk, kDevBounds);
+    return ok;
+  } else {
+    return true;
+  }
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
