@@ -13,15 +13,20 @@
 // takes the next one at once (longest-first list scheduling).  TMEM, the
 // mbarriers and the tensor-map prefetch are set up once per CTA; the
 // producer loads the next item's Q and K/V tiles while the current item
-// computes; and the MMA warp issues the next item's first Q K^T right behind
-// the current item's last P V, so a pair's epilogue (O / l and LSE read out
-// of TMEM and stored) overlaps the next pair's first products.
+// computes; and the next item's first Q K^T is issued right behind the
+// current item's last P V, so a pair's epilogue (O / l and LSE read out of
+// TMEM and stored) overlaps the next pair's first products.
 //
-// Roles (12 warps, as in the one-CTA-per-item kernel):
+// Roles (12 warps):
 //   warp 0      producer: takes items from the global counter into a
 //               two-entry ring in shared memory, loads Q tile 0, K_0, Q tile
 //               1, then K_{j+1} ahead of V_j through the K/V ring.
-//   warp 1      TMEM owner and MMA issuer (converged warp, elected lane).
+//   warp 1      TMEM owner; MMA issuer of query tile 0 (converged warp,
+//               elected lane).
+//   warp 2      MMA issuer of query tile 1.  Issuing an M = N = 128 product
+//               takes a warp about as long as the tensor pipe takes to run
+//               it, so with one issuing warp every wait of that warp left the
+//               pipe idle; two warps keep it fed while either one waits.
 //   warps 4-7   softmax and epilogue of query tile 0, warps 8-11 of tile 1.
 // Every phase counter (ring slots, S buffer, P and O hand-offs) runs on
 // across items.  The counter pair of the launch is reset by the last CTA to
@@ -58,20 +63,20 @@ struct FwdP {
   static constexpr int B_KVFULL = B_QEMPTY + 2;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2
-  static constexpr int B_SFREE = B_SFULL + 2;
-  static constexpr int B_PFULL = B_SFREE + 1;         // 2
+  static constexpr int B_SREAD = B_SFULL + 2;         // 2: S_t read out of the S buffer
+  static constexpr int B_PFULL = B_SREAD + 2;         // 2
   static constexpr int B_ODONE = B_PFULL + 2;         // 2
   static constexpr int B_ITFULL = B_ODONE + 2;        // IR: ring entry written
   static constexpr int B_ITEMPTY = B_ITFULL + IR;     // IR: ring entry read by every consumer warp
-  static constexpr int B_DRAIN = B_ITEMPTY + IR;
-  static constexpr int NBARS = B_DRAIN + 1;
+  static constexpr int B_DRAIN = B_ITEMPTY + IR;     // 2: one per issuing warp
+  static constexpr int NBARS = B_DRAIN + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_RING = OFF_ABORT + 4;
   static constexpr int RING_INTS = 8;                  // one decoded item per entry
   static constexpr int SMEM_BYTES = OFF_RING + 4 * RING_INTS * IR + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per block");
-  static constexpr int CONSUMER_WARPS = 1 + 8;  // MMA warp and the softmax warps
+  static constexpr int CONSUMER_WARPS = 2 + 8;  // the two MMA warps and the softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
   static constexpr uint32_t IDESC_O = idesc_bf16(kBM, D, false, true);
   static constexpr uint32_t TM_S = 0;
@@ -138,14 +143,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_KVFULL + s), 1);
-      mbar_init(bar(C::B_KVEMPTY + s), 1);
+      mbar_init(bar(C::B_KVEMPTY + s), 2);  // a K or V tile is read by both tiles' products
     }
     for (int r = 0; r < C::IR; ++r) {
       mbar_init(bar(C::B_ITFULL + r), 1);
       mbar_init(bar(C::B_ITEMPTY + r), C::CONSUMER_WARPS);
     }
-    mbar_init(bar(C::B_SFREE), 4);
-    mbar_init(bar(C::B_DRAIN), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_SREAD + t), 4);  // one arrival per softmax warp of tile t
+      mbar_init(bar(C::B_DRAIN + t), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -251,13 +258,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (qi[t] > 0) mbar_wait_drain(bar(C::B_QFULL + t), (qi[t] - 1) & 1, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
-      int li0 = 0;     // ring position of the current item's first K/V load
-      int qn = 0;      // items with Q loaded so far
-      int sfree = 0;   // SFREE completions waited for
-      bool first_s = true;
-      int pf[2] = {0, 0};  // PFULL completions waited for, per tile
+    } else if (warp == 1 || warp == 2) {
+      // ---------------------------------------------------------- MMA issuers
+      // Warp 1 issues query tile 0's products, warp 2 tile 1's.  A warp
+      // needs about as long to issue one M = N = 128 product as the tensor
+      // pipe needs to run it, so one issuing warp keeps the pipe busy only
+      // if it never waits; with two, either warp's products keep the pipe
+      // busy while the other waits.  Per tile: S_t(0), then for each j,
+      // S_t(j+1) ahead of P_t(j) V_j.  The one S buffer still alternates
+      // S_0(j), S_1(j), S_0(j+1): tile 1's S(j) waits until tile 0 has read
+      // S_0(j), tile 0's S(j+1) until tile 1 has read S_1(j).
+      const int t = warp - 1;
+      int li0 = 0;        // ring position of the current item's first K/V load
+      int qn = 0;         // items with Q loaded so far
+      int ns = 0;         // S products of this tile issued so far
+      int pf = 0;         // PFULL_t completions waited for
       bool ok = true;
       for (int it = 0; ok; ++it) {
         if (!wait_item(it)) break;
@@ -273,23 +288,23 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           return true;
         };
-        // Every S after the CTA's first waits until the S buffer has been read.
-        auto wait_sfree = [&]() -> bool {
-          if (first_s) {
-            first_s = false;
-            return true;
-          }
-          const bool r = mbar_wait_warp(bar(C::B_SFREE), sfree & 1, wc);
-          ++sfree;
-          return r;
+        // The S buffer is free for this tile's next S once the other tile
+        // has read the S issued before it: tile 1's ns-th S follows tile 0's
+        // ns-th, tile 0's ns-th follows tile 1's (ns - 1)-th.
+        auto wait_sbuf = [&]() -> bool {
+          if (t == 0 && ns == 0) return true;
+          const int phase = t == 0 ? ns - 1 : ns;
+          if (!mbar_wait_warp(bar(C::B_SREAD + (t ^ 1)), phase & 1, wc)) return false;
+          tc_fence_after();
+          return true;
         };
         // Descriptors of later K steps are the first one plus the byte
         // offset / 16 in the address field (shared addresses stay below
         // 256 KB, so the 14-bit field does not carry).
         // (The empty asm keeps the compiler from hoisting the CTA-constant Q
-        // descriptors of every K step out of the item loop: 32 registers the
-        // 72-register MMA warp does not have.)
-        auto issue_s = [&](int t, int j) {
+        // descriptors of every K step out of the item loop: registers the
+        // 72-register issuing warps do not have.)
+        auto issue_s = [&](int j) {
           uint64_t qd = sdesc_sw128(sQ + t * C::TILE_BYTES, 16, 1024);
           asm volatile("" : "+l"(qd));
           const uint64_t kd = sdesc_sw128(sKV + (k_li(j) % C::STAGES) * C::TILE_BYTES, 16, 1024);
@@ -299,69 +314,47 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss_warp(tmem + C::TM_S, qd + off16, kd + off16, C::IDESC_S, kk > 0 ? 1u : 0u);
           }
           tc_commit_warp(bar(C::B_SFULL + t));
-          if (j == n - 1) tc_commit_warp(bar(C::B_QEMPTY + t));                 // last reader of Q_t
-          if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + k_li(j) % C::STAGES));  // K_j read by both tiles
+          if (j == n - 1) tc_commit_warp(bar(C::B_QEMPTY + t));        // last reader of Q_t
+          tc_commit_warp(bar(C::B_KVEMPTY + k_li(j) % C::STAGES));    // one of K_j's two readers
+          ++ns;
         };
-        auto issue_pv = [&](int t, int j) {
+        auto issue_pv = [&](int j) {
           const uint64_t vd = sdesc_sw128(sKV + (v_li(j) % C::STAGES) * C::TILE_BYTES, C::BLOCK_BYTES, 1024);
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             mma_ts_warp(tmem + C::TM_O + t * D, tmem + C::TM_P + t * 64 + kk * 8, vd + (kk * 2048 >> 4),
                         C::IDESC_O, (kk > 0 || j > 0) ? 1u : 0u);
           tc_commit_warp(bar(C::B_ODONE + t));
-          if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + v_li(j) % C::STAGES));  // V_j read by both tiles
+          tc_commit_warp(bar(C::B_KVEMPTY + v_li(j) % C::STAGES));    // one of V_j's two readers
         };
-        auto wait_p = [&](int t) -> bool {
-          const bool r = mbar_wait_warp(bar(C::B_PFULL + t), pf[t] & 1, wc);
-          ++pf[t];
+        auto wait_p = [&]() -> bool {
+          const bool r = mbar_wait_warp(bar(C::B_PFULL + t), pf & 1, wc);
+          ++pf;
           if (r) tc_fence_after();
           return r;
         };
-        auto wait_q = [&](int t) -> bool { return mbar_wait_warp(bar(C::B_QFULL + t), qn & 1, wc); };
-        ok = wait_sfree() && wait_q(0) && wait_kv(k_li(0));
-        if (ok) issue_s(0, 0);
-        ok = ok && wait_sfree() && wait_q(1);
-        if (ok) {
-          tc_fence_after();
-          issue_s(1, 0);
-        }
-        if (ok && n > 1) {
-          ok = wait_sfree() && wait_kv(k_li(1));
-          if (ok) issue_s(0, 1);
-        }
+        ok = wait_sbuf() && mbar_wait_warp(bar(C::B_QFULL + t), qn & 1, wc) && wait_kv(k_li(0));
+        if (ok) issue_s(0);
         for (int j = 0; j < n && ok; ++j) {
-          if (!wait_kv(v_li(j)) || !wait_p(0)) {
-            ok = false;
-            break;
-          }
-          issue_pv(0, j);
           if (j + 1 < n) {
-            if (!wait_sfree()) {
+            if (!wait_sbuf() || !wait_kv(k_li(j + 1))) {
               ok = false;
               break;
             }
-            tc_fence_after();
-            issue_s(1, j + 1);
+            issue_s(j + 1);
           }
-          if (!wait_p(1)) {
+          if (!wait_kv(v_li(j)) || !wait_p()) {
             ok = false;
             break;
           }
-          issue_pv(1, j);
-          if (j + 2 < n) {
-            if (!wait_sfree() || !wait_kv(k_li(j + 2))) {
-              ok = false;
-              break;
-            }
-            issue_s(0, j + 2);
-          }
+          issue_pv(j);
         }
         li0 += 2 * n;
         ++qn;
       }
       // Drain: all MMAs of this warp complete before TMEM is released.
-      tc_commit_warp(bar(C::B_DRAIN));
-      mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
+      tc_commit_warp(bar(C::B_DRAIN + t));
+      mbar_wait_drain_warp(bar(C::B_DRAIN + t), 0, wc);
     }
   } else {
     regs_inc<kRegsHigh>();
@@ -412,7 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         reg_fence32(sr[3]);
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(bar(C::B_SFREE));
+        if (lane == 0) mbar_arrive(bar(C::B_SREAD + t));
         if ((k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qc0 + p.kv_off)) {
           const int lim = p.causal ? min(p.Nk - 1, qc + p.kv_off) : p.Nk - 1;
 #pragma unroll
