@@ -24,9 +24,10 @@
 //
 // Mapping (one CTA = two 128-row query tiles, 12 warps): warp 0 TMA producer
 // (Q tiles once, then K_j and Vt_j through an 8-slot ring), warp 1 TMEM
-// allocator and MMA issuer (S_t = Q_t K_j^T into one shared S buffer, O_t +=
-// P'_t Vt_j^T with P'_t in shared memory), warps 4..7 / 8..11 softmax of tile
-// 0 / 1, one row per thread.  TMEM: [0,128) S, [128,256) O_0, [256,384) O_1.
+// allocator and MMA issuer of tile 0, warp 2 MMA issuer of tile 1 (S_t = Q_t
+// K_j^T into one shared S buffer, O_t += P'_t Vt_j^T with P'_t in shared
+// memory), warps 4..7 / 8..11 softmax of tile 0 / 1, one row per thread.
+// TMEM: [0,128) S, [128,256) O_0, [256,384) O_1.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -136,11 +137,11 @@ struct F8 {
   static constexpr int B_KVFULL = 1;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2
-  static constexpr int B_SFREE = B_SFULL + 2;
-  static constexpr int B_PFULL = B_SFREE + 1;         // 2
+  static constexpr int B_SREAD = B_SFULL + 2;         // 2: S_t read out of the S buffer
+  static constexpr int B_PFULL = B_SREAD + 2;         // 2
   static constexpr int B_ODONE = B_PFULL + 2;         // 2
-  static constexpr int B_DRAIN = B_ODONE + 2;
-  static constexpr int NBARS = B_DRAIN + 1;
+  static constexpr int B_DRAIN = B_ODONE + 2;         // 2: one per issuing warp
+  static constexpr int NBARS = B_DRAIN + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int SMEM_BYTES = OFF_ABORT + 4 + 1024;
@@ -181,15 +182,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_KVFULL + s), 1);
-      mbar_init(bar(C::B_KVEMPTY + s), 1);
+      mbar_init(bar(C::B_KVEMPTY + s), 2);  // a K or V tile is read by both tiles' products
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::B_SFULL + i), 1);
       mbar_init(bar(C::B_PFULL + i), 4);
       mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_SFREE), 4);
-    mbar_init(bar(C::B_DRAIN), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::B_SREAD + t), 4);  // one arrival per softmax warp of tile t
+      mbar_init(bar(C::B_DRAIN + t), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -242,8 +245,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    } else if (warp == 1) {
-      // ---------------------------------------------------------- MMA issuer
+    } else if (warp == 1 || warp == 2) {
+      // ---------------------------------------------------------- MMA issuers
+      // Warp 1 issues query tile 0's products, warp 2 tile 1's (a warp needs
+      // about as long to issue one of these products as the tensor pipe
+      // needs to run it; two issuing warps keep the pipe fed while either
+      // waits).  Per tile: S_t(0), then S_t(j+1) ahead of P'_t(j) Vt_j.  The
+      // one S buffer alternates S_0(j), S_1(j), S_0(j+1): tile 1's S(j)
+      // waits until tile 0 has read S_0(j), tile 0's S(j+1) until tile 1 has
+      // read S_1(j).
+      const int t = warp - 1;
       auto k_li = [&](int j) -> int { return j == 0 ? 0 : 2 * j - 1; };
       auto v_li = [&](int j) -> int { return j == n_kv - 1 ? 2 * n_kv - 1 : 2 * j + 2; };
       auto kv_slot = [&](int li) -> int { return li % C::STAGES; };
@@ -253,8 +264,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         return true;
       };
+      int ns = 0;  // S products of this tile issued so far
+      auto wait_sbuf = [&]() -> bool {
+        if (t == 0 && ns == 0) return true;
+        const int phase = t == 0 ? ns - 1 : ns;
+        if (!mbar_wait_warp(bar(C::B_SREAD + (t ^ 1)), phase & 1, wc)) return false;
+        tc_fence_after();
+        return true;
+      };
       // S_t = Q_t K_j^T: four K = 32 steps along the 128-byte rows.
-      auto issue_s = [&](int t, int j) {
+      auto issue_s = [&](int j) {
         const uint32_t kb = sKV + kv_slot(k_li(j)) * C::TILE;
         const uint32_t qb = sQ + t * C::TILE;
 #pragma unroll
@@ -262,10 +281,11 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_f8_warp(tmem + C::TM_S, sdesc_sw128(qb + kk * 32, 16, 1024),
                          sdesc_sw128(kb + kk * 32, 16, 1024), C::IDESC, kk > 0 ? 1u : 0u);
         tc_commit_warp(bar(C::B_SFULL + t));
-        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));
+        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // one of K_j's two readers
+        ++ns;
       };
       // O_t += P'_t Vt_j^T: A = P'_t [query rows x keys], B = Vt_j [d rows x keys].
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int j) {
         const uint32_t vb = sKV + kv_slot(v_li(j)) * C::TILE;
         const uint32_t pb = sP + t * C::TILE;
 #pragma unroll
@@ -273,41 +293,21 @@ __global__ void __launch_bounds__(kThreads, 1)
           mma_ss_f8_warp(tmem + C::TM_O + t * 128, sdesc_sw128(pb + kk * 32, 16, 1024),
                          sdesc_sw128(vb + kk * 32, 16, 1024), C::IDESC, (kk > 0 || j > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_ODONE + t));
-        if (t == 1) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));
+        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // one of V_j's two readers
       };
-      int sfree = 0;
-      auto wait_sfree = [&]() -> bool {
-        const bool r = mbar_wait_warp(bar(C::B_SFREE), sfree & 1, wc);
-        ++sfree;
-        return r;
-      };
-      if (ok) ok = wait_kv(k_li(0));
-      if (ok) {
-        issue_s(0, 0);
-        ok = wait_sfree();
-      }
-      if (ok) issue_s(1, 0);
-      if (ok && n_kv > 1) ok = wait_sfree() && wait_kv(k_li(1));
-      if (ok && n_kv > 1) issue_s(0, 1);
+      if (ok) ok = wait_sbuf() && wait_kv(k_li(0));
+      if (ok) issue_s(0);
       for (int j = 0; j < n_kv && ok; ++j) {
-        if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + 0), j & 1, wc)) break;
-        tc_fence_after();
-        issue_pv(0, j);
         if (j + 1 < n_kv) {
-          if (!wait_sfree()) break;
-          tc_fence_after();
-          issue_s(1, j + 1);
+          if (!wait_sbuf() || !wait_kv(k_li(j + 1))) break;
+          issue_s(j + 1);
         }
-        if (!mbar_wait_warp(bar(C::B_PFULL + 1), j & 1, wc)) break;
+        if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + t), j & 1, wc)) break;
         tc_fence_after();
-        issue_pv(1, j);
-        if (j + 2 < n_kv) {
-          if (!wait_sfree() || !wait_kv(k_li(j + 2))) break;
-          issue_s(0, j + 2);
-        }
+        issue_pv(j);
       }
-      tc_commit_warp(bar(C::B_DRAIN));
-      mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
+      tc_commit_warp(bar(C::B_DRAIN + t));
+      mbar_wait_drain_warp(bar(C::B_DRAIN + t), 0, wc);
     }
   } else {
     regs_inc<kRegsHigh>();
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       reg_fence32(sr[3]);
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_SFREE));
+      if (lane == 0) mbar_arrive(bar(C::B_SREAD + t));
       if (k0 + kBN > p.N || (p.causal && k0 + kBN - 1 > qt0)) {
         const int lim = p.causal ? min(p.N - 1, q) : p.N - 1;
 #pragma unroll

@@ -69,11 +69,11 @@ struct Fwd {
   static constexpr int B_KVFULL = 1;
   static constexpr int B_KVEMPTY = B_KVFULL + STAGES;
   static constexpr int B_SFULL = B_KVEMPTY + STAGES;  // 2: S buffer holds S_t
-  static constexpr int B_SFREE = B_SFULL + 2;         // S buffer read out (either tile)
-  static constexpr int B_PFULL = B_SFREE + 1;         // 2
+  static constexpr int B_SREAD = B_SFULL + 2;         // 2: S_t read out of the S buffer
+  static constexpr int B_PFULL = B_SREAD + 2;         // 2
   static constexpr int B_ODONE = B_PFULL + 2;         // 2: P_t V complete
-  static constexpr int B_DRAIN = B_ODONE + 2;
-  static constexpr int NBARS = B_DRAIN + 1;
+  static constexpr int B_DRAIN = B_ODONE + 2;         // 2: one per issuing warp
+  static constexpr int NBARS = B_DRAIN + 2;
   static constexpr int OFF_TMEMSLOT = OFF_BAR + NBARS * 8;
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_NLIST = OFF_ABORT + 4;           // block-sparse: entries in the tile list
@@ -167,15 +167,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::B_QFULL), 1);
     for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(bar(C::B_KVFULL + s), 1);
-      mbar_init(bar(C::B_KVEMPTY + s), 1);
+      mbar_init(bar(C::B_KVEMPTY + s), two ? 2 : 1);  // one commit per tile reading the slot
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(C::B_SFULL + i), 1);
       mbar_init(bar(C::B_PFULL + i), 4);  // one arrival per softmax warp
       mbar_init(bar(C::B_ODONE + i), 1);
     }
-    mbar_init(bar(C::B_SFREE), 4);
-    mbar_init(bar(C::B_DRAIN), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar(C::B_SREAD + i), 4);  // one arrival per softmax warp of tile i
+      mbar_init(bar(C::B_DRAIN + i), 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -242,11 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
         mbar_wait_drain(bar(C::B_KVFULL + k % C::STAGES), (k / C::STAGES) & 1, wc);
-    } else if (warp == 1 && n_kv > 0) {
-      // ---------------------------------------------------------- MMA issuer
-      // The whole warp runs this loop (uniform operands); one elected lane issues.
+    } else if ((warp == 1 || (two && warp == 2)) && n_kv > 0) {
+      // ---------------------------------------------------------- MMA issuers
+      // The whole warp runs this loop (uniform operands); one elected lane
+      // issues.  Two query tiles: warp 1 issues tile 0's products and warp 2
+      // tile 1's (a warp needs about as long to issue an M = N = 128 product
+      // as the tensor pipe needs to run it, so two issuing warps keep the
+      // pipe fed while either waits).  One tile: warp 1 alone.
       // Ring slots of the loads (see the producer): K_0 first, then K_{j+1}
       // ahead of V_j.
+      const int t = warp - 1;
       auto k_li = [&](int j) -> int { return j == 0 ? 0 : 2 * j - 1; };
       auto v_li = [&](int j) -> int { return j == n_kv - 1 ? 2 * n_kv - 1 : 2 * j + 2; };
       auto kv_slot = [&](int li) -> int { return li % C::STAGES; };
@@ -257,7 +264,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         return true;
       };
       // S_t = Q_t K_j^T into the shared S buffer.
-      auto issue_s = [&](int t, int j) {
+      auto issue_s = [&](int j) {
         const uint32_t kb = sKV + kv_slot(k_li(j)) * C::TILE_BYTES;
         const uint32_t qb = sQ + t * C::TILE_BYTES;
 #pragma unroll
@@ -267,10 +274,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                       C::IDESC_S, kk > 0 ? 1u : 0u);
         }
         tc_commit_warp(bar(C::B_SFULL + t));
-        if (t == 1 || !two) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // K_j read by every tile
+        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(k_li(j))));  // K_j: one commit per tile
       };
       // O_t += P_t V_j (A = 16 keys of P_t = 8 TMEM columns; B = 16 V rows, MN-major).
-      auto issue_pv = [&](int t, int j) {
+      auto issue_pv = [&](int j) {
         const uint32_t vb = sKV + kv_slot(v_li(j)) * C::TILE_BYTES;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk)
@@ -278,61 +285,43 @@ __global__ void __launch_bounds__(kThreads, 1)
                       sdesc_sw128(vb + kk * 2048, C::BLOCK_BYTES, 1024), C::IDESC_O,
                       (kk > 0 || j > 0) ? 1u : 0u);
         tc_commit_warp(bar(C::B_ODONE + t));
-        if (t == 1 || !two) tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // V_j read by every tile
+        tc_commit_warp(bar(C::B_KVEMPTY + kv_slot(v_li(j))));  // V_j: one commit per tile
       };
-      // The S buffer passes between the tiles: S_0(j), S_1(j), S_0(j+1), ...
-      // Each S is issued once the previous one has been read out (SFREE).
-      int sfree = 0;  // completions of SFREE waited for so far
-      auto wait_sfree = [&]() -> bool {
-        const bool r = mbar_wait_warp(bar(C::B_SFREE), sfree & 1, wc);
-        ++sfree;
-        return r;
+      // The S buffer passes S_0(j), S_1(j), S_0(j+1), ... (one tile: S_0(j),
+      // S_0(j+1), ...); each S is issued once the one before it has been
+      // read: tile 1's S(j) after tile 0 read S_0(j), tile 0's S(j) after
+      // tile 1 (one tile: tile 0) read the previous one.
+      int ns = 0;  // S products of this tile issued so far
+      auto wait_sbuf = [&]() -> bool {
+        if (t == 0 && ns == 0) return true;
+        const int other = two ? t ^ 1 : 0;
+        const int phase = (t == 0) ? ns - 1 : ns;
+        if (!mbar_wait_warp(bar(C::B_SREAD + other), phase & 1, wc)) return false;
+        tc_fence_after();
+        return true;
       };
-      if (ok) ok = wait_kv(k_li(0));
-      if (ok && !two) {
-        // Tile 0 alone: S_0(j+1) as soon as S_0(j) has been read (P_0 has its
-        // own columns), then P_0 V_j.
-        issue_s(0, 0);
-        for (int j = 0; j < n_kv && ok; ++j) {
-          if (j + 1 < n_kv) {
-            if (!wait_sfree() || !wait_kv(k_li(j + 1))) break;
-            issue_s(0, j + 1);
-          }
-          if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + 0), j & 1, wc)) break;
-          tc_fence_after();
-          issue_pv(0, j);
-        }
-        ok = false;  // the two-tile schedule below does not run
-      }
+      auto wait_p = [&](int j) -> bool {
+        if (!mbar_wait_warp(bar(C::B_PFULL + t), j & 1, wc)) return false;
+        tc_fence_after();
+        return true;
+      };
+      ok = ok && wait_sbuf() && wait_kv(k_li(0));
       if (ok) {
-        issue_s(0, 0);
-        ok = wait_sfree();
+        issue_s(0);
+        ++ns;
       }
-      if (ok) issue_s(1, 0);
-      if (ok && n_kv > 1) ok = wait_sfree() && wait_kv(k_li(1));
-      if (ok && n_kv > 1) issue_s(0, 1);
       for (int j = 0; j < n_kv && ok; ++j) {
-        // P_0(j) ready -> O_0 += P_0 V_j.  The S buffer then holds S_0(j+1);
-        // once tile 0 has read it, S_1(j+1) follows.
-        if (!wait_kv(v_li(j)) || !mbar_wait_warp(bar(C::B_PFULL + 0), j & 1, wc)) break;
-        tc_fence_after();
-        issue_pv(0, j);
         if (j + 1 < n_kv) {
-          if (!wait_sfree()) break;
-          tc_fence_after();
-          issue_s(1, j + 1);
+          if (!wait_sbuf() || !wait_kv(k_li(j + 1))) break;
+          issue_s(j + 1);
+          ++ns;
         }
-        if (!mbar_wait_warp(bar(C::B_PFULL + 1), j & 1, wc)) break;
-        tc_fence_after();
-        issue_pv(1, j);
-        if (j + 2 < n_kv) {
-          if (!wait_sfree() || !wait_kv(k_li(j + 2))) break;
-          issue_s(0, j + 2);
-        }
+        if (!wait_kv(v_li(j)) || !wait_p(j)) break;
+        issue_pv(j);
       }
       // Drain: all MMAs of this warp complete before TMEM is released.
-      tc_commit_warp(bar(C::B_DRAIN));
-      mbar_wait_drain_warp(bar(C::B_DRAIN), 0, wc);
+      tc_commit_warp(bar(C::B_DRAIN + t));
+      mbar_wait_drain_warp(bar(C::B_DRAIN + t), 0, wc);
     }
   } else {
     regs_inc<kRegsHigh>();
@@ -372,7 +361,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The S buffer can take the other tile's next scores now.
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(bar(C::B_SFREE));
+      if (lane == 0) mbar_arrive(bar(C::B_SREAD + t));
       // Mask keys past N (ragged tail) and, on tiles crossing the diagonal, keys after q.
       if (!on || (k0 + kBN > p.Nk) || (p.causal && k0 + kBN - 1 > qc0 + p.kv_off)) {
         const int lim = !on ? -1 : p.causal ? min(p.Nk - 1, qc + p.kv_off) : p.Nk - 1;
@@ -549,19 +538,20 @@ size_t fwd_bf16_smem_bytes(int d) {
   return d == 128 ? Fwd<128>::SMEM_BYTES : Fwd<64>::SMEM_BYTES;
 }
 
+// Rows <= 128 (one query tile), or a block mask.  The dense two-tile case
+// runs in the persistent kernel (launch_fwd_persist).
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream) {
   const bool one = p.rows <= kBM, m = p.bmask != nullptr;
+  if (!one && !m) return cudaErrorInvalidValue;
   if (d == 128)
     return one ? (m ? launch_one<128, true, true>(tmQ, tmK, tmV, p, stream)
                     : launch_one<128, true, false>(tmQ, tmK, tmV, p, stream))
-               : (m ? launch_one<128, false, true>(tmQ, tmK, tmV, p, stream)
-                    : launch_one<128, false, false>(tmQ, tmK, tmV, p, stream));
+               : launch_one<128, false, true>(tmQ, tmK, tmV, p, stream);
   if (d == 64)
     return one ? (m ? launch_one<64, true, true>(tmQ, tmK, tmV, p, stream)
                     : launch_one<64, true, false>(tmQ, tmK, tmV, p, stream))
-               : (m ? launch_one<64, false, true>(tmQ, tmK, tmV, p, stream)
-                    : launch_one<64, false, false>(tmQ, tmK, tmV, p, stream));
+               : launch_one<64, false, true>(tmQ, tmK, tmV, p, stream);
   return cudaErrorInvalidValue;
 }
 

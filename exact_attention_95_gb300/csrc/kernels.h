@@ -48,8 +48,9 @@ struct FwdParams {
 // not share one.
 unsigned* sched_counter_pair();
 
-// tcgen05 forward for bf16 inputs.  tmQ/tmK/tmV are 3-D maps over
-// [B*H][N][d] with a (64, 128, 1) box and 128-byte swizzle.
+// tcgen05 forward for bf16 inputs with one query tile (rows <= 128) or a
+// block mask.  tmQ/tmK/tmV are 3-D maps over [B*H][N][d] with a (64, 128, 1)
+// box and 128-byte swizzle.
 cudaError_t launch_fwd_bf16(int d, const CUtensorMap& tmQ, const CUtensorMap& tmK,
                             const CUtensorMap& tmV, const FwdParams& p, cudaStream_t stream);
 size_t fwd_bf16_smem_bytes(int d);
