@@ -371,7 +371,7 @@ def run_native(args):
     if main_avg >= fwd_avg:
         dom, dom_tf = "bwd_main_kernel (attn_bwd_main)", main_tf
     else:
-        dom, dom_tf = "fwd_bf16_kernel (attn_fwd)", fwd_tf
+        dom, dom_tf = "fwd_persist_kernel (attn_fwd)", fwd_tf
     traffic = load_traffic(dom, args.workload)
     peak, peak_desc = tensor_peak(peaks, peak_src, wall)
     roofline = {"bound": "tensor", "achieved": dom_tf, "peak": peak, "unit": "TFLOP/s",
@@ -866,7 +866,7 @@ def load_traffic(kernel_desc, workload):
     elif kernel_desc.startswith("fwd_fp8"):
         key, src = "fwd_fp8", "fp8.cu"
     else:
-        key, src = "fwd", "fwd_sm103.cu"
+        key, src = "fwd", "fwd_persist.cu"
     ent = d.get(key)
     if not ent or ent.get("workload") != workload or ent.get("source_sha256") != kernel_source_sha(src):
         return None
