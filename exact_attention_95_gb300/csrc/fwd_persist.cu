@@ -74,7 +74,10 @@ struct FwdP {
   static constexpr int OFF_ABORT = OFF_TMEMSLOT + 4;
   static constexpr int OFF_RING = OFF_ABORT + 4;
   static constexpr int RING_INTS = 8;                  // one decoded item per entry
-  static constexpr int SMEM_BYTES = OFF_RING + 4 * RING_INTS * IR + 1024;  // + alignment slack
+  // Epilogue staging: per softmax warp, its 32 rows x 64 columns of bf16 O.
+  static constexpr int EPI_WARP_BYTES = 32 * 128;
+  static constexpr int OFF_EPI = (OFF_RING + 4 * RING_INTS * IR + 127) / 128 * 128;
+  static constexpr int SMEM_BYTES = OFF_EPI + 8 * EPI_WARP_BYTES + 1024;  // + alignment slack
   static_assert(SMEM_BYTES <= 232448, "exceeds the 227 KB of shared memory per block");
   static constexpr int CONSUMER_WARPS = 2 + 8;  // the two MMA warps and the softmax warps
   static constexpr uint32_t IDESC_S = idesc_bf16(kBM, kBN, false, false);
@@ -231,7 +234,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         e[R_BHKV] = w.bh_kv;
         e[R_SPLIT] = w.split;
         mbar_arrive(bar(C::B_ITFULL + r));
-        if (k < 0) break;
+        if (k < 0) {
+          // No item left: a merge launched behind this kernel may start (it
+          // waits for this kernel's completion before reading).
+          griddep_launch_dependents();
+          break;
+        }
         const int n = w.n_kv;
         if (n == 0) continue;
         // Use order: Q_0, K_0, Q_1, then K_{j+1} ahead of V_j.
@@ -366,6 +374,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t s_t = tmem + lane_off + C::TM_S;
     const uint32_t p_t = tmem + lane_off + C::TM_P + t * 64;
     const uint32_t o_t = tmem + lane_off + C::TM_O + t * D;
+    const uint32_t sEpi = sb + C::OFF_EPI + (warp - 4) * C::EPI_WARP_BYTES;
     const float sl2 = p.scale_log2;
     // S tiles of this warpgroup completed so far (SFULL_t phases).  Each
     // tile but an item's first waits for the previous P_t V, and the
@@ -502,7 +511,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       const float lo = l - corr;
       const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
       const int bh = e[R_BH];
-      const bool valid = q < p.rows && dcheck(bh >= 0 && bh < p.heads && split >= 0 && split < p.n_splits, p.status);
+      const bool bh_ok = dcheck(bh >= 0 && bh < p.heads && split >= 0 && split < p.n_splits, p.status);
+      const bool valid = q < p.rows && bh_ok;
       const size_t row_idx = (size_t)bh * p.rows + q;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
@@ -522,17 +532,35 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(o_out16 + row_idx * D + c * 32);
+            // bf16: the row's 32 columns go to this warp's staging rows
+            // (128 bytes per row, 16-byte chunk k at position k ^ (row & 7));
+            // after each 64-column half the warp stores its 32 rows with
+            // coalesced 16-byte stores, four whole rows per instruction.
+            const uint32_t srow = sEpi + lane * 128;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[i] = v;
+              const int k = (c & 1) * 4 + i;
+              sts_u4(srow + ((k ^ (lane & 7)) << 4),
+                     pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
+                     pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
             }
           }
+        }
+        if (!p.out_f32 && (c & 1)) {
+          __syncwarp();
+          const int h = c >> 1;  // 64-column half of the row
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int r = 4 * i + (lane >> 3);  // staging row = row - quad * 32
+            const int k = lane & 7;
+            const uint4 v = lds_u4(sEpi + r * 128 + ((k ^ (r & 7)) << 4));
+            const int qr = qt0 + quad * 32 + r;
+            if (qr < p.rows && bh_ok)
+              *reinterpret_cast<uint4*>(o_out16 + ((size_t)bh * p.rows + qr) * D + h * 64 + k * 8) = v;
+          }
+          __syncwarp();
         }
       }
       if (valid) {

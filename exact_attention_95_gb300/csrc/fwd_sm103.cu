@@ -240,6 +240,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_3d(sKV + s * C::TILE_BYTES + cb * C::BLOCK_BYTES, m, bar(C::B_KVFULL + s), cb * 64,
                         kt * kBN, bh_kv);
       }
+      // All loads are issued: a merge launched behind this kernel may start
+      // (it waits for this kernel's completion before reading).
+      griddep_launch_dependents();
       // Drain: every issued copy must land before the CTA may exit.
       mbar_wait_drain(bar(C::B_QFULL), 0, wc);
       for (int k = max(0, li - C::STAGES); k < li; ++k)
