@@ -446,12 +446,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (lane == 0) mbar_arrive(bar(C::B_PFULL + t));
     }
     // Epilogue: O = max(sv) O' / (l - corr), LSE = (m - shift + log2 l) ln 2.
-    if (ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc)) {
+    // bf16 rows go out through this warp's quarter of the tile's P' buffer,
+    // free once the tile's last P' V has completed.  The staging needs the
+    // whole warp: a warp some of whose lanes gave up (a timed-out wait, already
+    // in the status word) writes nothing.
+    const bool ep = ok && mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc);
+    if (__all_sync(0xffffffffu, ep)) {
       tc_fence_after();
       const float lo = l - corr;
       const float inv_l = lo > 0.f ? svm / lo : 0.f;
       const bool valid = q < p.N;
       const size_t row_idx = (size_t)bh * p.N + q;
+      const uint32_t sEpi = sP + t * C::TILE + quad * 4096;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -465,18 +471,12 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.O) + row_idx * 128 + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[i] = v;
-            }
+            epi_stage32(sEpi, lane, c, o, inv_l);
           }
         }
+        if (!p.out_f32 && (c & 1))
+          epi_store_half(sEpi, lane, c >> 1, static_cast<uint16_t*>(p.O), (size_t)bh * p.N + qt0 + quad * 32, 128,
+                         p.N - (qt0 + quad * 32));
       }
       if (valid) p.LSE[row_idx] = (l > 0.f) ? (m - kShift + lg2(l)) * 0.69314718055994531f : -INFINITY;
     }

@@ -532,36 +532,13 @@ __global__ void __launch_bounds__(kThreads, 1)
               dst[i] = make_float4(__uint_as_float(o[4 * i]) * inv_l, __uint_as_float(o[4 * i + 1]) * inv_l,
                                    __uint_as_float(o[4 * i + 2]) * inv_l, __uint_as_float(o[4 * i + 3]) * inv_l);
           } else {
-            // bf16: the row's 32 columns go to this warp's staging rows
-            // (128 bytes per row, 16-byte chunk k at position k ^ (row & 7));
-            // after each 64-column half the warp stores its 32 rows with
-            // coalesced 16-byte stores, four whole rows per instruction.
-            const uint32_t srow = sEpi + lane * 128;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int k = (c & 1) * 4 + i;
-              sts_u4(srow + ((k ^ (lane & 7)) << 4),
-                     pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l),
-                     pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l));
-            }
+            epi_stage32(sEpi, lane, c, o, inv_l);
           }
         }
-        if (!p.out_f32 && (c & 1)) {
-          __syncwarp();
-          const int h = c >> 1;  // 64-column half of the row
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int r = 4 * i + (lane >> 3);  // staging row = row - quad * 32
-            const int k = lane & 7;
-            const uint4 v = lds_u4(sEpi + r * 128 + ((k ^ (r & 7)) << 4));
-            const int qr = qt0 + quad * 32 + r;
-            if (qr < p.rows && bh_ok)
-              *reinterpret_cast<uint4*>(o_out16 + ((size_t)bh * p.rows + qr) * D + h * 64 + k * 8) = v;
-          }
-          __syncwarp();
-        }
+        // bf16: after each 64-column half, the warp stores its 32 rows.
+        if (!p.out_f32 && (c & 1))
+          epi_store_half(sEpi, lane, c >> 1, o_out16, (size_t)bh * p.rows + qt0 + quad * 32, D,
+                         bh_ok ? p.rows - (qt0 + quad * 32) : 0);
       }
       if (valid) {
         float* const lse_out = p.LSE + split * p.lse_split_stride;

@@ -456,15 +456,22 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     // Epilogue: O / l and LSE (O = 0, LSE = -inf when no key was in range).
     const bool have = n_kv > 0;
-    if (ok && active && (!have || mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc))) {
+    const bool ep = ok && active && (!have || mbar_wait(bar(C::B_ODONE + t), (n_kv - 1) & 1, wc));
+    // bf16 rows go out through this warp's quarter of its Q tile, free once
+    // the tile's last P V -- and with it every product of the tile -- has
+    // completed.  The staging needs the whole warp: a warp some of whose lanes
+    // gave up (a timed-out wait, already in the status word) writes nothing.
+    if (__all_sync(0xffffffffu, ep)) {
       if (have) tc_fence_after();
       // O is divided by the row sum less the rounding of each tile's largest
       // P: when one key dominates a row, its bf16 rounding then cancels
       // between O and the divisor.  LSE uses the exact sum.
       const float lo = l - corr;
       const float inv_l = lo > 0.f ? 1.f / lo : 0.f;
-      const bool valid = q < p.rows && dcheck(split < p.n_splits, p.status);
+      const bool split_ok = dcheck(split < p.n_splits, p.status);
+      const bool valid = q < p.rows && split_ok;
       const size_t row_idx = (size_t)bh * p.rows + q;
+      const uint32_t sEpi = sQ + t * C::TILE_BYTES + quad * 4096;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t o[32];
@@ -484,18 +491,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                                    __uint_as_float(o[4 * i + 2]) * inv_l,
                                    __uint_as_float(o[4 * i + 3]) * inv_l);
           } else {
-            uint4* dst = reinterpret_cast<uint4*>(o_out16 + row_idx * D + c * 32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              uint4 v;
-              v.x = pack_bf16(__uint_as_float(o[8 * i + 0]) * inv_l, __uint_as_float(o[8 * i + 1]) * inv_l);
-              v.y = pack_bf16(__uint_as_float(o[8 * i + 2]) * inv_l, __uint_as_float(o[8 * i + 3]) * inv_l);
-              v.z = pack_bf16(__uint_as_float(o[8 * i + 4]) * inv_l, __uint_as_float(o[8 * i + 5]) * inv_l);
-              v.w = pack_bf16(__uint_as_float(o[8 * i + 6]) * inv_l, __uint_as_float(o[8 * i + 7]) * inv_l);
-              dst[i] = v;
-            }
+            epi_stage32(sEpi, lane, c, o, inv_l);
           }
         }
+        if (!p.out_f32 && (c & 1))
+          epi_store_half(sEpi, lane, c >> 1, o_out16, (size_t)bh * p.rows + qt0 + quad * 32, D,
+                         split_ok ? p.rows - (qt0 + quad * 32) : 0);
       }
       if (valid) {
         // LSE = ln(sum_j e^{s_j}) = (m + log2 l) * ln 2, m in log2 units.

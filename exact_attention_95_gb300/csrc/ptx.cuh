@@ -339,6 +339,42 @@ __device__ __forceinline__ void sts_u4(uint32_t addr, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// Epilogue stores of bf16 rows through shared memory.  Thread = row: lane l
+// holds row l of its warp's 32 rows, 32 columns at a time.  A warp's 64-column
+// half of its rows is staged in 32 x 128 bytes (16-byte chunk k of row r at
+// position k ^ (r & 7): conflict-free both ways) and stored with coalesced
+// 16-byte stores, four whole 128-byte row pieces per instruction, instead of
+// 16-byte pieces of 32 different rows.
+// Stage chunk c (columns 32c .. 32c+31) of this lane's row, scaled by mul.
+__device__ __forceinline__ void epi_stage32(uint32_t stage, int lane, int c, const uint32_t (&o)[32], float mul) {
+  const uint32_t srow = stage + lane * 128;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int k = (c & 1) * 4 + i;
+    sts_u4(srow + ((k ^ (lane & 7)) << 4),
+           pack_bf16(__uint_as_float(o[8 * i + 0]) * mul, __uint_as_float(o[8 * i + 1]) * mul),
+           pack_bf16(__uint_as_float(o[8 * i + 2]) * mul, __uint_as_float(o[8 * i + 3]) * mul),
+           pack_bf16(__uint_as_float(o[8 * i + 4]) * mul, __uint_as_float(o[8 * i + 5]) * mul),
+           pack_bf16(__uint_as_float(o[8 * i + 6]) * mul, __uint_as_float(o[8 * i + 7]) * mul));
+  }
+}
+// Store the staged half h (columns 64h .. 64h+63) of the warp's rows: row r
+// goes to out + (row0 + r) * ld, for r < nvalid.  Call with the whole warp
+// after both chunks of the half are staged; it synchronises the warp before
+// and after.
+__device__ __forceinline__ void epi_store_half(uint32_t stage, int lane, int h, uint16_t* out, size_t row0,
+                                               int ld, int nvalid) {
+  __syncwarp();
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const int r = 4 * i + (lane >> 3);
+    const int k = lane & 7;
+    const uint4 v = lds_u4(stage + r * 128 + ((k ^ (r & 7)) << 4));
+    if (r < nvalid) *reinterpret_cast<uint4*>(out + (row0 + r) * (size_t)ld + h * 64 + k * 8) = v;
+  }
+  __syncwarp();
+}
+
 // Warpgroup register reallocation (all four warps of a warpgroup execute it).
 template <int N>
 __device__ __forceinline__ void regs_dec() {
