@@ -177,10 +177,11 @@ class ClockSampler:
 # ---------------------------------------------------------------- oracle timing
 def oracle_step(w, t64, n_tokens: int, head: int):
     """fp64 oracle forward + backward on the causal prefix [0, n_tokens) of one
-    head of the workload; returns (seconds, convention FLOPs credited)."""
+    head of batch 0 of the workload (the tensors hold batch 0 only; heads
+    wrap around); returns (seconds, convention FLOPs credited)."""
     import numpy as np
     import oracle
-    b, h = divmod(head % (w.B * w.Hq), w.Hq)
+    b, h = 0, head % w.Hq
     hk = h // (w.Hq // w.Hkv)
     sl = slice(0, n_tokens)
     Q = np.ascontiguousarray(t64["Q"][b:b + 1, h:h + 1, sl])

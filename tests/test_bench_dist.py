@@ -62,3 +62,16 @@ def test_reference_arm_other_ranks_exit(monkeypatch):
     monkeypatch.setenv("RANK", "1")
     monkeypatch.setenv("WORLD_SIZE", "2")
     assert bench.run_reference(bench.parse_args(["--impl", "reference"])) == 0
+
+
+def test_oracle_step_wraps_heads_within_batch_zero():
+    # The reference arm samples batch 0 only; a step index past its heads
+    # (long --steps runs) must wrap to another head of batch 0.
+    import types
+    import numpy as np
+    rng = np.random.default_rng(5)
+    w = types.SimpleNamespace(B=2, Hq=2, Hkv=1, N=64, d=16, scale=0.25, causal=True)
+    t64 = {k: rng.standard_normal((1, w.Hq if k in ("Q", "dO") else w.Hkv, w.N, w.d)) for k in ("Q", "K", "V", "dO")}
+    for head in (0, 1, 2, 5, 301):
+        dt, fl = bench.oracle_step(w, t64, 64, head)
+        assert dt >= 0 and fl == 3.5 * 4.0 * 64 * 64 * 16 / 2
