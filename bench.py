@@ -206,6 +206,7 @@ def oracle_tensors(w):
 def size_oracle_sample(w, t64, budget_s: float) -> int:
     """Prefix length whose oracle step takes about budget_s (cost ~ n^2)."""
     n0 = 512
+    oracle_step(w, t64, 64, 0)  # loads (and if needed builds) the oracle library first
     dt, _ = oracle_step(w, t64, n0, 0)
     n = int(n0 * math.sqrt(max(budget_s, 1e-3) / max(dt, 1e-6)))
     return max(64, min(w.N, n // 64 * 64))
