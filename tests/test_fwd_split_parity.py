@@ -67,6 +67,10 @@ CASES = [
     (1, 2, 2, 8, 300, 128, True, 2),      # Hq == Hkv, 8 rows, bottom-right causal
     (1, 6, 2, 2, 2000, 128, True, 0),     # 6 packed rows
     (1, 4, 2, 1, 1, 128, False, 0),       # a single key
+    # More parts than one warp's lanes: the merge reads the parts' LSEs in
+    # chunks of 32 and their O rows in batches of 16.
+    (1, 4, 2, 2, 9000, 64, True, 40),
+    (1, 2, 1, 1, 9000, 128, False, 71),
 ]
 
 
