@@ -45,6 +45,65 @@ EncodeTiledFn encode_fn() {
   return fn;
 }
 
+// cuTensorMapEncodeTiled through a small cache keyed by every argument that
+// enters the encoding (a map holds the address and the geometry, nothing of
+// the contents, so a hit is exactly the map a new encoding would give).
+// Repeated calls on the same buffers -- a training or decoding loop -- skip
+// the host-side encoding.  64 entries, replaced in turn; one mutex.
+struct MapKey {
+  int dtype, rank, swizzle;
+  uintptr_t base;
+  cuuint64_t dims[3], strides[2];
+  cuuint32_t box[3];
+  bool operator==(const MapKey& o) const {
+    if (dtype != o.dtype || rank != o.rank || swizzle != o.swizzle || base != o.base) return false;
+    for (int i = 0; i < 3; ++i)
+      if (dims[i] != o.dims[i] || box[i] != o.box[i]) return false;
+    return strides[0] == o.strides[0] && strides[1] == o.strides[1];
+  }
+};
+
+bool encode_tiled(CUtensorMap* m, CUtensorMapDataType dtype, int rank, const void* base, const cuuint64_t* dims,
+                  const cuuint64_t* strides, const cuuint32_t* box, CUtensorMapSwizzle swizzle) {
+  constexpr int kEntries = 64;
+  static MapKey keys[kEntries];
+  static CUtensorMap maps[kEntries];
+  static bool used[kEntries] = {};
+  static int next = 0;
+  static std::mutex mu;
+  MapKey k{};
+  k.dtype = (int)dtype;
+  k.rank = rank;
+  k.swizzle = (int)swizzle;
+  k.base = reinterpret_cast<uintptr_t>(base);
+  for (int i = 0; i < rank; ++i) {
+    k.dims[i] = dims[i];
+    k.box[i] = box[i];
+    if (i + 1 < rank) k.strides[i] = strides[i];
+  }
+  {
+    std::lock_guard<std::mutex> lk(mu);
+    for (int i = 0; i < kEntries; ++i)
+      if (used[i] && keys[i] == k) {
+        *m = maps[i];
+        return true;
+      }
+  }
+  EncodeTiledFn fn = encode_fn();
+  if (!fn) return false;
+  const cuuint32_t estr[3] = {1, 1, 1};
+  if (fn(m, dtype, (cuuint32_t)rank, const_cast<void*>(base), dims, strides, box, estr,
+         CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+    return false;
+  std::lock_guard<std::mutex> lk(mu);
+  keys[next] = k;
+  maps[next] = *m;
+  used[next] = true;
+  next = (next + 1) % kEntries;
+  return true;
+}
+
 // Device address of the status word on the current device.
 int* status_ptr() {
   static int* ptrs[64] = {};
@@ -97,44 +156,29 @@ int sm_count() {
 // 3-D map over a bf16 [BH][N][d] tensor: box of 64 columns (128 bytes, the
 // 128-byte swizzle width) x box_rows rows x 1 head.  Rows past N read as zero.
 bool make_map(CUtensorMap* m, const void* base, long long BH, int N, int d, int box_rows) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
-  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
-  cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box,
-            estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)N, (cuuint64_t)BH};
+  const cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)N * d * 2};
+  const cuuint32_t box[3] = {64, (cuuint32_t)box_rows, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // 2-D fp32 map over the backward's dQ accumulator [rows][d]: box (d, 64), no
 // swizzle; the target of bulk reduce-adds of 64-row tiles.
 bool make_acc_map(CUtensorMap* m, const void* base, long long rows, int d) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)d * 4};
-  cuuint32_t box[2] = {(cuuint32_t)d, 64};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[2] = {(cuuint64_t)d, (cuuint64_t)rows};
+  const cuuint64_t strides[1] = {(cuuint64_t)d * 4};
+  const cuuint32_t box[2] = {(cuuint32_t)d, 64};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_NONE);
 }
 
 // 3-D map over uint8 e4m3 codes [planes][rows][cols] (row stride `ld` bytes):
 // box of 128 bytes x 128 rows x 1 plane, 128-byte swizzle.  Reads past the
 // extents return zero.
 bool make_map_u8(CUtensorMap* m, const void* base, long long planes, int rows, int cols, long long ld) {
-  EncodeTiledFn fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
-  cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)ld * rows};
-  cuuint32_t box[3] = {128, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+  const cuuint64_t dims[3] = {(cuuint64_t)cols, (cuuint64_t)rows, (cuuint64_t)planes};
+  const cuuint64_t strides[2] = {(cuuint64_t)ld, (cuuint64_t)ld * rows};
+  const cuuint32_t box[3] = {128, 128, 1};
+  return encode_tiled(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, base, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
