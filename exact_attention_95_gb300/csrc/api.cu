@@ -17,8 +17,10 @@ __device__ int g_status = 0;
 
 // Work counters of persistent launches: kSchedPairs pairs (next item, CTAs
 // finished) per device, 0 between launches (each launch's last CTA resets its
-// pair).  Launches take pairs in turn, so up to kSchedPairs launches may be
-// in flight at once (on any streams) without sharing a pair.
+// pair).  A pair belongs to a stream: launches on one stream run one after
+// the other and reuse it; up to kSchedPairs streams per device get pairs of
+// their own (a further stream takes over the pair of the stream seen longest
+// ago).
 constexpr int kSchedPairs = 64;
 __device__ unsigned g_sched[2 * kSchedPairs];
 
@@ -121,8 +123,10 @@ int* status_ptr() {
 
 }  // namespace
 
-unsigned* sched_counter_pair() {
+unsigned* sched_counter_pair(cudaStream_t stream) {
   static unsigned* base[64] = {};
+  static cudaStream_t owner[64][kSchedPairs] = {};
+  static bool taken[64][kSchedPairs] = {};
   static unsigned next[64] = {};
   static std::mutex mu;
   int dev = 0;
@@ -133,9 +137,12 @@ unsigned* sched_counter_pair() {
     if (cudaGetSymbolAddress(&p, g_sched) != cudaSuccess) return nullptr;
     base[dev] = static_cast<unsigned*>(p);
   }
-  unsigned* pair = base[dev] + 2 * (next[dev] % kSchedPairs);
-  ++next[dev];
-  return pair;
+  for (int i = 0; i < kSchedPairs; ++i)
+    if (taken[dev][i] && owner[dev][i] == stream) return base[dev] + 2 * i;
+  const int i = (int)(next[dev]++ % kSchedPairs);
+  owner[dev][i] = stream;
+  taken[dev][i] = true;
+  return base[dev] + 2 * i;
 }
 
 namespace {
@@ -331,7 +338,7 @@ attn_status fwd_bf16_run(const void* Q, const void* K, const void* V, void* O, f
     // Dense two-tile forward: persistent, one CTA per SM (its shared memory
     // and TMEM allow one) over the items.
     const int sms = sm_count();
-    p.sched = sched_counter_pair();
+    p.sched = sched_counter_pair(s);
     if (sms < 1 || !p.sched) return ATTN_ERR_CUDA;
     p.n_items = (int)(heads * p.n_pairs * splits);
     e = launch_fwd_persist(d, tq, tk, tv, p, std::min(p.n_items, sms), s);

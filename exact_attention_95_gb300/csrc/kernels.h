@@ -43,10 +43,10 @@ struct FwdParams {
   int n_items;
 };
 
-// Counter pairs for persistent launches: a launch takes the next pair of a
-// small per-device pool, so that launches in flight on different streams do
-// not share one.
-unsigned* sched_counter_pair();
+// Counter pair for a persistent launch on `stream`: each stream has its own
+// pair from a per-device pool of 64 (launches on one stream run in order and
+// share it; launches on different streams may run at once and do not).
+unsigned* sched_counter_pair(cudaStream_t stream);
 
 // tcgen05 forward for bf16 inputs with one query tile (rows <= 128) or a
 // block mask.  tmQ/tmK/tmV are 3-D maps over [B*H][N][d] with a (64, 128, 1)

@@ -28,7 +28,14 @@
  * default stream.  Every call is asynchronous on that stream.  Argument and
  * launch errors are returned synchronously; a device-side failure (a bounded
  * wait inside a kernel that ran out) is recorded in a device status word and
- * reported by attn_last_device_status().
+ * reported by attn_last_device_status().  Calls on different streams may run
+ * at the same time: the dense forward with more than 128 query rows runs
+ * persistent CTAs that take work items from a pair of device counters, and
+ * each stream has a pair of its own (64 per device; a 65th stream takes over
+ * the pair of the stream seen longest ago, so keep at most 64 streams per
+ * device issuing such forwards at once).  A captured graph holds its stream's
+ * pair: do not replay it concurrently with itself or with calls on the
+ * stream it was captured from.
  *
  * Errors: ATTN_ERR_INVALID_ARG for null or misaligned pointers, non-positive
  * sizes, Hq % Hkv != 0, a scale that is not finite and positive, or an
