@@ -7,8 +7,11 @@
 //
 // Block: 128 threads.  TPR = d/32 consecutive threads share one query row,
 // each holding 32 of its d components of q and of the output accumulator.
-// Keys are streamed in tiles of 32 through shared memory; the partial dot
-// products of a row's TPR threads are combined with warp shuffles.
+// Keys are streamed in tiles of 32 through shared memory (the next tile's
+// loads are in flight in registers while the current one is used) and read
+// back as float4: the threads of a warp read at most TPR distinct addresses
+// at a time (broadcasts), so rows need no padding.  The partial dot products
+// of a row's TPR threads are combined with warp shuffles.
 #include "kernels.h"
 #include "ptx.cuh"
 
@@ -23,10 +26,10 @@ __global__ void __launch_bounds__(128)
                    const float* __restrict__ V, float* __restrict__ O, float* __restrict__ LSE,
                    int Hq, int Hkv, int N, float sl2, int causal) {
   constexpr int TPR = D / 32;
-  constexpr int RPB = 128 / TPR;  // rows per block
-  constexpr int PAD = 33;         // padded 32-float segment (avoids bank conflicts)
-  __shared__ float Ks[kKT][TPR * PAD];
-  __shared__ float Vs[kKT][TPR * PAD];
+  constexpr int RPB = 128 / TPR;           // rows per block
+  constexpr int PER = kKT * D / 4 / 128;   // float4 of K (and of V) per thread and tile
+  __shared__ __align__(16) float Ks[kKT][D];
+  __shared__ __align__(16) float Vs[kKT][D];
 
   const int bh = blockIdx.y;
   const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
@@ -46,24 +49,45 @@ __global__ void __launch_bounds__(128)
   float m = -INFINITY, l = 0.f;
   const int q_last = min(N - 1, blockIdx.x * RPB + RPB - 1);
   const int kend = causal ? q_last + 1 : N;
-  const float* Kh = K + (size_t)bh_kv * N * D;
-  const float* Vh = V + (size_t)bh_kv * N * D;
-  for (int k0 = 0; k0 < kend; k0 += kKT) {
-    __syncthreads();
-    for (int idx = threadIdx.x; idx < kKT * D; idx += 128) {
-      const int kr = idx / D, c = idx - (idx / D) * D;
+  const float4* Kh = reinterpret_cast<const float4*>(K + (size_t)bh_kv * N * D);
+  const float4* Vh = reinterpret_cast<const float4*>(V + (size_t)bh_kv * N * D);
+  float4 pk[PER], pv[PER];
+  auto load_tile = [&](int k0) {
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int idx = threadIdx.x + i * 128;  // float4 index within the tile
+      const int kr = idx / (D / 4);
       const bool in = k0 + kr < N;
-      Ks[kr][(c / 32) * PAD + (c % 32)] = in ? Kh[(size_t)(k0 + kr) * D + c] : 0.f;
-      Vs[kr][(c / 32) * PAD + (c % 32)] = in ? Vh[(size_t)(k0 + kr) * D + c] : 0.f;
+      const size_t g = (size_t)k0 * (D / 4) + idx;
+      pk[i] = in ? Kh[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+      pv[i] = in ? Vh[g] : make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  };
+  load_tile(0);
+  for (int k0 = 0; k0 < kend; k0 += kKT) {
+    __syncthreads();  // the previous tile has been read
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int idx = threadIdx.x + i * 128;
+      reinterpret_cast<float4*>(&Ks[0][0])[idx] = pk[i];
+      reinterpret_cast<float4*>(&Vs[0][0])[idx] = pv[i];
     }
     __syncthreads();
+    if (k0 + kKT < kend) load_tile(k0 + kKT);  // lands while this tile is used
     float s[kKT];
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kKT; ++j) {
+      const float4* kr4 = reinterpret_cast<const float4*>(&Ks[j][sub * 32]);
       float part = 0.f;
 #pragma unroll
-      for (int k = 0; k < 32; ++k) part = fmaf(qv[k], Ks[j][sub * PAD + k], part);
+      for (int k4 = 0; k4 < 8; ++k4) {
+        const float4 kv = kr4[k4];
+        part = fmaf(qv[4 * k4 + 0], kv.x, part);
+        part = fmaf(qv[4 * k4 + 1], kv.y, part);
+        part = fmaf(qv[4 * k4 + 2], kv.z, part);
+        part = fmaf(qv[4 * k4 + 3], kv.w, part);
+      }
 #pragma unroll
       for (int o = 1; o < TPR; o <<= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
       const int key = k0 + j;
@@ -81,8 +105,15 @@ __global__ void __launch_bounds__(128)
     for (int j = 0; j < kKT; ++j) {
       const float pj = ex2(s[j] - m_use);
       rs += pj;
+      const float4* vr4 = reinterpret_cast<const float4*>(&Vs[j][sub * 32]);
 #pragma unroll
-      for (int k = 0; k < 32; ++k) acc[k] = fmaf(pj, Vs[j][sub * PAD + k], acc[k]);
+      for (int k4 = 0; k4 < 8; ++k4) {
+        const float4 vv = vr4[k4];
+        acc[4 * k4 + 0] = fmaf(pj, vv.x, acc[4 * k4 + 0]);
+        acc[4 * k4 + 1] = fmaf(pj, vv.y, acc[4 * k4 + 1]);
+        acc[4 * k4 + 2] = fmaf(pj, vv.z, acc[4 * k4 + 2]);
+        acc[4 * k4 + 3] = fmaf(pj, vv.w, acc[4 * k4 + 3]);
+      }
     }
     l = l * alpha + rs;
     m = m_new;
