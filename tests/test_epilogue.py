@@ -76,3 +76,20 @@ def test_fp8_bf16_equals_rounded_fp32():
         O32, L32 = pkg.attn_fwd_fp8(qc, qs, kc, ks, vc, vs, None, causal, out_dtype=torch.float32)
         O16, L16 = pkg.attn_fwd_fp8(qc, qs, kc, ks, vc, vs, None, causal)
         _same(O32, L32, O16, L16)
+
+
+def test_tensor_map_cache_follows_shape():
+    # The library caches TMA tensor maps by every encoding argument: the same
+    # base pointer with another length must not reuse the longer map.
+    t = make(1, 1, 1, 900, 128, seed=0xE9D0, names=("Q", "K", "V"))
+    g = {k: to_dev(v) for k, v in t.items()}
+    full = pkg.attn_fwd(g["Q"], g["K"], g["V"], None, True, out_dtype=torch.float32)
+    for n in (900, 333, 129, 900):
+        pre = {k: v[:, :, :n] for k, v in g.items()}  # contiguous prefix views, same base pointers
+        fresh = {k: v.clone() for k, v in pre.items()}
+        a = pkg.attn_fwd(pre["Q"], pre["K"], pre["V"], None, True, out_dtype=torch.float32)
+        b = pkg.attn_fwd(fresh["Q"], fresh["K"], fresh["V"], None, True, out_dtype=torch.float32)
+        torch.cuda.synchronize()
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+        # Causal: a prefix of the queries sees exactly the same keys.
+        assert torch.equal(a[0], full[0][:, :, :n]) and torch.equal(a[1], full[1][:, :, :n])
