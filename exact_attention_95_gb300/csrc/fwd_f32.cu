@@ -5,37 +5,55 @@
 // carried out entirely in fp32 FFMA so that fp32 inputs keep fp32 accuracy.
 // The work is small (latency-bound); the kernel favours simplicity.
 //
-// Block: 128 threads.  TPR = d/32 consecutive threads share one query row,
-// each holding 32 of its d components of q and of the output accumulator.
-// Keys are streamed in tiles of 32 through shared memory (the next tile's
-// loads are in flight in registers while the current one is used) and read
-// back as float4: the threads of a warp read at most TPR distinct addresses
-// at a time (broadcasts), so rows need no padding.  The partial dot products
-// of a row's TPR threads are combined with warp shuffles.
+// Block: 256 threads in two groups of 128 that take alternate key tiles of
+// the same query rows (a row's work is a chain over its keys; two chains per
+// row halve it) and merge their (m, l, O) at the end as two blocks of the
+// online softmax.  In a group, TPR = d/32 consecutive threads share one query
+// row, each holding 32 of its d components of q and of the output
+// accumulator.  Keys are streamed in tiles of 32 through the group's shared
+// memory (the next tile's loads are in flight in registers while the current
+// one is used) and read back as float4: the threads of a warp read at most
+// TPR distinct addresses at a time (broadcasts), so rows need no padding.
+// The partial dot products of a row's TPR threads are combined with warp
+// shuffles.
 #include "kernels.h"
 #include "ptx.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kKT = 32;  // keys per shared-memory tile
+constexpr int kKT = 32;      // keys per shared-memory tile
+constexpr int kGroups = 2;   // key-tile groups per block
+constexpr int kF32Threads = 128 * kGroups;
 
 template <int D>
-__global__ void __launch_bounds__(128)
+constexpr int f32_smem_bytes() {
+  return kGroups * 2 * kKT * D * 4;  // K and V tiles per group
+}
+
+__device__ __forceinline__ void group_sync(int grp) {
+  asm volatile("bar.sync %0, %1;" ::"r"(1 + grp), "r"(128) : "memory");
+}
+
+template <int D>
+__global__ void __launch_bounds__(kF32Threads)
     fwd_f32_kernel(const float* __restrict__ Q, const float* __restrict__ K,
                    const float* __restrict__ V, float* __restrict__ O, float* __restrict__ LSE,
                    int Hq, int Hkv, int N, float sl2, int causal) {
   constexpr int TPR = D / 32;
   constexpr int RPB = 128 / TPR;           // rows per block
   constexpr int PER = kKT * D / 4 / 128;   // float4 of K (and of V) per thread and tile
-  __shared__ __align__(16) float Ks[kKT][D];
-  __shared__ __align__(16) float Vs[kKT][D];
+  extern __shared__ float4 f32_smem[];
+  const int grp = threadIdx.x >> 7;
+  const int tid = threadIdx.x & 127;
+  float* const Ks = reinterpret_cast<float*>(f32_smem) + grp * 2 * kKT * D;  // [kKT][D]
+  float* const Vs = Ks + kKT * D;
 
   const int bh = blockIdx.y;
   const int b = bh / Hq, h = bh - (bh / Hq) * Hq;
   const int bh_kv = b * Hkv + h / (Hq / Hkv);
-  const int sub = threadIdx.x % TPR;
-  const int r = threadIdx.x / TPR;
+  const int sub = tid % TPR;
+  const int r = tid / TPR;
   const int q = blockIdx.x * RPB + r;
   const bool valid = q < N;
   const size_t qrow = (size_t)bh * N + (valid ? q : 0);
@@ -55,7 +73,7 @@ __global__ void __launch_bounds__(128)
   auto load_tile = [&](int k0) {
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int idx = threadIdx.x + i * 128;  // float4 index within the tile
+      const int idx = tid + i * 128;  // float4 index within the tile
       const int kr = idx / (D / 4);
       const bool in = k0 + kr < N;
       const size_t g = (size_t)k0 * (D / 4) + idx;
@@ -63,22 +81,23 @@ __global__ void __launch_bounds__(128)
       pv[i] = in ? Vh[g] : make_float4(0.f, 0.f, 0.f, 0.f);
     }
   };
-  load_tile(0);
-  for (int k0 = 0; k0 < kend; k0 += kKT) {
-    __syncthreads();  // the previous tile has been read
+  const int k_first = grp * kKT;
+  if (k_first < kend) load_tile(k_first);
+  for (int k0 = k_first; k0 < kend; k0 += kGroups * kKT) {
+    group_sync(grp);  // the previous tile has been read
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
-      const int idx = threadIdx.x + i * 128;
-      reinterpret_cast<float4*>(&Ks[0][0])[idx] = pk[i];
-      reinterpret_cast<float4*>(&Vs[0][0])[idx] = pv[i];
+      const int idx = tid + i * 128;
+      reinterpret_cast<float4*>(Ks)[idx] = pk[i];
+      reinterpret_cast<float4*>(Vs)[idx] = pv[i];
     }
-    __syncthreads();
-    if (k0 + kKT < kend) load_tile(k0 + kKT);  // lands while this tile is used
+    group_sync(grp);
+    if (k0 + kGroups * kKT < kend) load_tile(k0 + kGroups * kKT);  // lands while this tile is used
     float s[kKT];
     float mx = -INFINITY;
 #pragma unroll
     for (int j = 0; j < kKT; ++j) {
-      const float4* kr4 = reinterpret_cast<const float4*>(&Ks[j][sub * 32]);
+      const float4* kr4 = reinterpret_cast<const float4*>(Ks + j * D + sub * 32);
       float part = 0.f;
 #pragma unroll
       for (int k4 = 0; k4 < 8; ++k4) {
@@ -105,7 +124,7 @@ __global__ void __launch_bounds__(128)
     for (int j = 0; j < kKT; ++j) {
       const float pj = ex2(s[j] - m_use);
       rs += pj;
-      const float4* vr4 = reinterpret_cast<const float4*>(&Vs[j][sub * 32]);
+      const float4* vr4 = reinterpret_cast<const float4*>(Vs + j * D + sub * 32);
 #pragma unroll
       for (int k4 = 0; k4 < 8; ++k4) {
         const float4 vv = vr4[k4];
@@ -118,11 +137,32 @@ __global__ void __launch_bounds__(128)
     l = l * alpha + rs;
     m = m_new;
   }
-  if (valid) {
-    const float inv = l > 0.f ? 1.f / l : 0.f;
+  // Merge the two groups' (m, l, O) per row ("LLM 注意力与计算内核精读笔记 ·
+  // 02 FlashAttention" §5): group 1 hands its partial results to group 0
+  // through shared memory (the tiles are no longer needed).
+  __syncthreads();
+  float* const part = reinterpret_cast<float*>(f32_smem);  // [128 threads][34]
+  if (grp == 1) {
+    float* dst = part + tid * 34;
+    dst[0] = m;
+    dst[1] = l;
 #pragma unroll
-    for (int k = 0; k < 32; ++k) O[qrow * D + sub * 32 + k] = acc[k] * inv;
-    if (sub == 0) LSE[qrow] = l > 0.f ? (m + lg2(l)) * 0.69314718055994531f : -INFINITY;
+    for (int k = 0; k < 32; ++k) dst[2 + k] = acc[k];
+  }
+  __syncthreads();
+  if (grp == 0) {
+    const float* src = part + tid * 34;
+    const float m1 = src[0], l1 = src[1];
+    const float mt = fmaxf(m, m1);
+    const float mu = mt == -INFINITY ? 0.f : mt;
+    const float a0 = ex2(m - mu), a1 = ex2(m1 - mu);
+    const float lt = a0 * l + a1 * l1;
+    if (valid) {
+      const float inv = lt > 0.f ? 1.f / lt : 0.f;
+#pragma unroll
+      for (int k = 0; k < 32; ++k) O[qrow * D + sub * 32 + k] = (a0 * acc[k] + a1 * src[2 + k]) * inv;
+      if (sub == 0) LSE[qrow] = lt > 0.f ? (mt + lg2(lt)) * 0.69314718055994531f : -INFINITY;
+    }
   }
 }
 
@@ -133,12 +173,22 @@ cudaError_t launch_fwd_f32(int d, const float* Q, const float* K, const float* V
                            int causal, cudaStream_t stream) {
   const int rpb = 128 / (d / 32);
   dim3 grid((N + rpb - 1) / rpb, B * Hq);
-  if (d == 64)
-    fwd_f32_kernel<64><<<grid, 128, 0, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
-  else if (d == 128)
-    fwd_f32_kernel<128><<<grid, 128, 0, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
-  else
+  cudaError_t e;
+  if (d == 64) {
+    constexpr int smem = f32_smem_bytes<64>();
+    static_assert(smem >= 128 * 34 * 4, "merge buffer");
+    e = cudaFuncSetAttribute(fwd_f32_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fwd_f32_kernel<64><<<grid, kF32Threads, smem, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
+  } else if (d == 128) {
+    constexpr int smem = f32_smem_bytes<128>();
+    static_assert(smem >= 128 * 34 * 4, "merge buffer");
+    e = cudaFuncSetAttribute(fwd_f32_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return e;
+    fwd_f32_kernel<128><<<grid, kF32Threads, smem, stream>>>(Q, K, V, O, LSE, Hq, Hkv, N, scale_log2, causal);
+  } else {
     return cudaErrorInvalidValue;
+  }
   return cudaGetLastError();
 }
 
